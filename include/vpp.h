@@ -1,0 +1,221 @@
+/*
+ * vpp.h -- C ABI of the GB300 (sm_103a) chunked-prefill causal-attention library.
+ *
+ * The operation is one chunked-prefill step of causal self-attention: a chunk
+ * of C query tokens whose first token sits at absolute position P (the prefix
+ * length) attends to every cached key/value at positions 0 .. P + i
+ * (inclusive) for its i-th token.  Citations name the pages by title:
+ *
+ *   [VPP review]   "VPP: Virtual Pipeline Parallelism for Efficient Chunked
+ *                  Prefill in Long-Context LLM Inference" (English technical
+ *                  review): §2.1 (prefill fills the KV cache, decode reads
+ *                  it), §2.2 Eq. (1) (softmax(Q K^T / sqrt(d)) V, token i
+ *                  attends to tokens <= i), §2.3 (chunked prefill: a later
+ *                  chunk attends to the whole cached prefix plus itself).
+ *   [GLM PP note]  "02 · 并行策略与 PP 切分" (deployment note): §1 (paged KV
+ *                  pool, block_size = 64), §7 (context-parallel attention
+ *                  needs the backend to return the LSE of each partial).
+ *   [FastPP summary] "Revisiting Pipeline Parallelism for LLM Serving":
+ *                  section "预备知识：分块与三种气泡" (a micro-batch mixes
+ *                  prefill chunks with one-token decode requests).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every tensor argument is caller-owned DEVICE memory unless the
+ *           argument says HOST.  The library allocates no device memory in
+ *           any call; scratch space is the caller's `workspace`.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *           default stream).  Calls enqueue work and return without
+ *           synchronising.  A launch failure returns VPP_ERR_CUDA.
+ * Layouts.  Row-major, contiguous, 16-byte aligned base pointers.
+ *             q, out        [T][heads][d]          (token-major)
+ *             lse           [heads][T] float32, natural log of the softmax
+ *                           denominator, ln sum_j exp(s_j)
+ *             paged cache   k_cache [num_blocks][64][kv_heads][head_dim_qk]
+ *                           v_cache [num_blocks][64][kv_heads][head_dim_v]
+ *                           token j of a sequence lives in block
+ *                           block_table[j / 64], row j % 64
+ *             contiguous    k_cache [capacity][kv_heads][head_dim_qk]
+ *                           (block_table == NULL); v_cache likewise
+ *           bf16 means IEEE bfloat16 stored as uint16.
+ * Heads.    GQA: query head h reads kv head h / (heads / kv_heads).
+ *           heads == kv_heads is plain multi-head attention.
+ * Scale.    softmax_scale <= 0 selects 1 / sqrt(head_dim_qk) ([VPP review]
+ *           Eq. (1), d read as the per-head query/key dimension).
+ * Supported head_dim_qk in {64, 128, 192}, head_dim_v in {64, 128},
+ *           heads / kv_heads in {1, 2, 4, 8, 16}; anything else returns
+ *           VPP_ERR_UNSUPPORTED.
+ * Errors.   Arguments are validated on the host before any launch; nothing
+ *           is enqueued when a call returns an error.  Kernels never trap: a
+ *           wait that times out on the device records VPP_ERR_TIMEOUT in a
+ *           device status word that vpp_last_device_status() reads.
+ */
+#ifndef VPP_H
+#define VPP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VPP_OK = 0,
+    VPP_ERR_INVALID = -1,     /* bad pointer, size, alignment or range       */
+    VPP_ERR_UNSUPPORTED = -2, /* valid but unsupported head dims / grouping  */
+    VPP_ERR_CUDA = -3,        /* a CUDA runtime call failed                  */
+    VPP_ERR_TIMEOUT = -4,     /* a device-side wait ran out (status word)    */
+    VPP_ERR_WORKSPACE = -5    /* workspace missing or smaller than required  */
+} vpp_status;
+
+typedef enum {
+    VPP_BF16 = 0,
+    VPP_FP32 = 1
+} vpp_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *vpp_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int vpp_version(void);
+
+/*
+ * a1 -- KV append ([VPP review] §2.1: prefill fills the cache that later
+ * chunks and decode read; [GLM PP note] §1: 64-token blocks).
+ *
+ * Copies the chunk's new keys k_new [chunk_len][kv_heads][head_dim_qk] and
+ * values v_new [chunk_len][kv_heads][head_dim_v] into cache positions
+ * prefix_len .. prefix_len + chunk_len - 1.  in_dtype is the type of
+ * k_new/v_new: VPP_BF16 is a bit copy; VPP_FP32 is rounded to bf16
+ * (round-to-nearest-even) on the way in.  The cache is always bf16.
+ * block_table (device int32, >= ceil((prefix_len+chunk_len)/64) entries, each
+ * in [0, num_blocks)) selects the paged layout; NULL selects the contiguous
+ * layout, where num_blocks is instead the capacity in tokens.
+ * Block-table entries are not read on the host; out-of-range entries are
+ * skipped on the device and recorded as VPP_ERR_INVALID in the status word.
+ * chunk_len == 0 is a no-op returning VPP_OK.
+ */
+int vpp_kv_append(const void *k_new, const void *v_new, int in_dtype,
+                  void *k_cache, void *v_cache, const int32_t *block_table,
+                  int32_t num_blocks, int64_t prefix_len, int64_t chunk_len,
+                  int kv_heads, int head_dim_qk, int head_dim_v, void *stream);
+
+/*
+ * a2..a6 -- chunk attention, the plain form: contiguous bf16 cache
+ * [prefix_len + chunk_len][kv_heads][head_dim], head_dim_qk = head_dim_v =
+ * head_dim, default scale, no key splitting (no workspace).
+ *
+ * q [chunk_len][heads][head_dim] bf16 -> out [chunk_len][heads][head_dim]
+ * bf16 and lse [heads][chunk_len] float32 (lse may be NULL).  Query i
+ * attends keys 0 .. prefix_len + i of the cache ([VPP review] §2.2 Eq. (1),
+ * §2.3).  The chunk's own K/V must already be in the cache (vpp_kv_append
+ * first).  chunk_len == 0 is a no-op.
+ */
+int vpp_chunk_attn(const void *q, const void *k_cache, const void *v_cache,
+                   int64_t prefix_len, int64_t chunk_len, int heads,
+                   int kv_heads, int head_dim, void *out, float *lse,
+                   void *stream);
+
+/*
+ * a2..a7 -- chunk attention, full form.
+ *
+ * q_dtype: VPP_BF16, or VPP_FP32 (q is then rounded to bf16 into the
+ * workspace before the attention kernel reads it).  Cache as described in
+ * the conventions (paged if block_table != NULL, num_blocks = blocks in the
+ * pool; contiguous otherwise, num_blocks = capacity in tokens, which must be
+ * >= prefix_len + chunk_len).
+ * num_splits: 0 lets the library choose; 1 forbids splitting; S > 1 asks
+ * for S key ranges over the prefix (clamped so every range is non-empty).
+ * With more than one range, each range writes a float32 partial (output,
+ * lse) into the workspace and a merge kernel combines them
+ * ([GLM PP note] §7):  L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) out_s.
+ * workspace: device scratch of at least vpp_chunk_attn_workspace_size(...)
+ * bytes for the same arguments (NULL allowed when that size is 0).
+ * out [chunk_len][heads][head_dim_v] bf16, lse [heads][chunk_len] float32
+ * (NULL allowed).
+ */
+int vpp_chunk_attn_ex(const void *q, int q_dtype, const void *k_cache,
+                      const void *v_cache, const int32_t *block_table,
+                      int32_t num_blocks, int64_t prefix_len,
+                      int64_t chunk_len, int heads, int kv_heads,
+                      int head_dim_qk, int head_dim_v, float softmax_scale,
+                      int num_splits, void *out, float *lse, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Workspace bytes vpp_chunk_attn_ex needs for these arguments (0 if none). */
+size_t vpp_chunk_attn_workspace_size(int q_dtype, int64_t prefix_len,
+                                     int64_t chunk_len, int heads,
+                                     int kv_heads, int head_dim_qk,
+                                     int head_dim_v, int num_splits);
+
+/* The number of key ranges vpp_chunk_attn_ex will use for these arguments. */
+int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len,
+                              int heads, int kv_heads, int head_dim_qk,
+                              int head_dim_v, int num_splits);
+
+/*
+ * a8..a9 -- mixed micro-batch: prefill chunks and one-token decode rows over
+ * one paged cache ([FastPP summary] "预备知识"; [VPP review] §2.1).
+ *
+ * q [total_q][heads][head_dim_qk] bf16, where sequence b owns rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and its queries are its LAST
+ * q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] positions: prefix
+ * ctx_lens[b] - q_len_b.  ctx_lens[b] counts the sequence's own new tokens,
+ * which must already be in the cache.  q_len_b == 1 is a decode row (split-KV
+ * decode kernel); q_len_b > 1 is a prefill chunk (chunk-attention kernel);
+ * q_len_b == 0 is skipped.
+ * cu_seqlens_q [batch+1] and ctx_lens [batch] are HOST int32 arrays (the
+ * plan is built on the host and passed to the kernels by value; batch <=
+ * 1024).  block_table is a device int32 [batch][max_blocks_per_seq].
+ * out [total_q][heads][head_dim_v] bf16, lse [heads][total_q] float32 (NULL
+ * allowed).  workspace >= vpp_mixed_attn_workspace_size(...) bytes.
+ */
+int vpp_mixed_attn(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_table, int32_t max_blocks_per_seq,
+                   int32_t num_blocks, const int32_t *cu_seqlens_q,
+                   const int32_t *ctx_lens, int32_t batch, int heads,
+                   int kv_heads, int head_dim_qk, int head_dim_v,
+                   float softmax_scale, void *out, float *lse,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes vpp_mixed_attn needs (HOST cu_seqlens_q / ctx_lens). */
+size_t vpp_mixed_attn_workspace_size(const int32_t *cu_seqlens_q,
+                                     const int32_t *ctx_lens, int32_t batch,
+                                     int heads, int kv_heads, int head_dim_qk,
+                                     int head_dim_v);
+
+/*
+ * Varlen KV append for a mixed batch: the new K/V rows of every sequence,
+ * packed like q in vpp_mixed_attn ([total_q][kv_heads][d]), go to the last
+ * q_len_b positions of sequence b (HOST cu_seqlens_q / ctx_lens, device
+ * block_table [batch][max_blocks_per_seq]).  bf16 in, bf16 cache.
+ */
+int vpp_kv_append_varlen(const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_table,
+                         int32_t max_blocks_per_seq, int32_t num_blocks,
+                         const int32_t *cu_seqlens_q, const int32_t *ctx_lens,
+                         int32_t batch, int kv_heads, int head_dim_qk,
+                         int head_dim_v, void *stream);
+
+/*
+ * Device status word: synchronises `stream`, stores the first error any
+ * kernel of this library recorded since the last reset (VPP_OK if none) in
+ * *code, and resets the word to VPP_OK.  Returns VPP_ERR_CUDA if the
+ * synchronisation or copy fails.
+ */
+int vpp_last_device_status(void *stream, int *code);
+
+/*
+ * Self-test of the bounded device wait: launches one block that waits on a
+ * shared-memory barrier nothing will ever complete, giving up after
+ * timeout_us microseconds (1 .. 5,000,000).  The wait must run out and record
+ * VPP_ERR_TIMEOUT in the status word; the context stays usable.
+ */
+int vpp_selftest_wait_timeout(int timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VPP_H */
