@@ -1,0 +1,507 @@
+// api.cu -- the C ABI of include/vpp.h: argument validation, TMA tensor maps,
+// work planning and kernel launches.  Allocates no device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "chunk_attn.cuh"
+#include "common.cuh"
+#include "vpp.h"
+
+namespace vpp {
+__device__ int g_status_word;  // first device-side error since the last read
+}
+
+using namespace vpp;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[64];
+EncodeTiledFn g_encode = nullptr;
+
+// One-time, per-device set-up: SM count, status-word address, driver entry
+// point of cuTensorMapEncodeTiled.  Thread-safe.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VPP_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return VPP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return VPP_ERR_CUDA;
+    if (major != 10 || minor != 3) return VPP_ERR_UNSUPPORTED;  // built for sm_103a only
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_status_word) != cudaSuccess)
+      return VPP_ERR_CUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          fn == nullptr)
+        return VPP_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return VPP_OK;
+}
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+bool supported_dims(int dq, int dv) {
+  return (dq == 64 || dq == 128 || dq == 192) && (dv == 64 || dv == 128);
+}
+
+int check_heads(int heads, int kv_heads) {
+  if (heads <= 0 || kv_heads <= 0 || heads % kv_heads != 0) return VPP_ERR_INVALID;
+  const int g = heads / kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return VPP_ERR_UNSUPPORTED;
+  return VPP_OK;
+}
+
+// bf16 tensor map with 128-byte swizzle; an out-of-range box reads zeros.
+int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box) {
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+                              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VPP_OK : VPP_ERR_INVALID;
+}
+
+// Q (and any [T][heads][d] tensor) viewed as [T][kv_heads][G][d]; a box is
+// 64 dims x G heads x 1 kv head x 128/G tokens = 128 rows of 128 bytes.
+int make_q_map(CUtensorMap* m, const void* q, int64_t total_q, int heads, int kv_heads, int dq) {
+  const int G = heads / kv_heads;
+  const cuuint64_t dims[4] = {(cuuint64_t)dq, (cuuint64_t)G, (cuuint64_t)kv_heads,
+                              (cuuint64_t)total_q};
+  const cuuint64_t strides[3] = {(cuuint64_t)dq * 2, (cuuint64_t)G * dq * 2,
+                                 (cuuint64_t)heads * dq * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(kTileM / G)};
+  return encode_map(m, q, 4, dims, strides, box);
+}
+
+// Paged cache [num_blocks][64][kv_heads][d]: box = 64 dims x 1 head x 64 rows x 1 block.
+int make_paged_map(CUtensorMap* m, const void* cache, int32_t num_blocks, int kv_heads, int d) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)kv_heads, (cuuint64_t)kBlockTokens,
+                              (cuuint64_t)num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)kv_heads * d * 2,
+                                 (cuuint64_t)kBlockTokens * kv_heads * d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBlockTokens, 1};
+  return encode_map(m, cache, 4, dims, strides, box);
+}
+
+// Contiguous cache [n_tokens][kv_heads][d]; rows past n_tokens read zeros.
+int make_contig_map(CUtensorMap* m, const void* cache, int64_t n_tokens, int kv_heads, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)kv_heads, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)kv_heads * d * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlockTokens};
+  return encode_map(m, cache, 3, dims, strides, box);
+}
+
+struct SplitPlan {
+  int n_splits;
+  int split_keys;
+};
+
+int pairs_for(int64_t q_len, int group) { return (int)ceil_div(q_len, 2 * (kTileM / group)); }
+
+// Chooses the number of key ranges for one chunk.  The model: a CTA costs its
+// key count plus a fixed ~256 keys of prologue/epilogue; CTAs run in waves of
+// num_sms; a split adds a float32 round trip of the partials through HBM.
+SplitPlan plan_splits(int64_t P, int64_t C, int heads, int kv_heads, int dv, int requested,
+                      int num_sms) {
+  SplitPlan none{1, 0};
+  if (requested == 1 || P < kTileN || C <= 0) return none;
+  const int G = heads / kv_heads;
+  const int64_t base = (int64_t)pairs_for(C, G) * kv_heads;
+  int S = requested;
+  if (requested <= 0) {
+    const double key_ns = 8.5;  // one key of one CTA (two 128-row tiles, d = 128)
+    double best = 1e300;
+    S = 1;
+    for (int s = 1; s <= 16; ++s) {
+      if (s > 1 && P / s < 512) break;
+      const double waves = std::ceil((double)(base * s) / num_sms);
+      double t = waves * ((double)P / s + 0.5 * C + 256.0) * key_ns;
+      if (s > 1) t += (double)(s + 1) * C * heads * dv * 4.0 / 5.0e3;  // ns at ~5 TB/s
+      if (t < best * 0.98) {
+        best = t;
+        S = s;
+      }
+    }
+  }
+  S = std::min(S, 16);
+  if (S <= 1) return none;
+  const int64_t keys = round_up((size_t)ceil_div(P, S), (size_t)kTileN);
+  const int64_t S_eff = std::min<int64_t>(S, P / keys + 1);
+  if (S_eff <= 1) return none;
+  return SplitPlan{(int)S_eff, (int)keys};
+}
+
+size_t ws_q_bytes(int q_dtype, int64_t C, int heads, int dq) {
+  return q_dtype == VPP_FP32 ? round_up((size_t)C * heads * dq * 2, 256) : 0;
+}
+
+size_t ws_split_bytes(int S, int64_t C, int heads, int dv) {
+  if (S <= 1) return 0;
+  return round_up((size_t)S * C * heads * dv * 4, 256) + round_up((size_t)S * C * heads * 4, 256);
+}
+
+int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                    const int32_t* block_table, int32_t num_blocks, int64_t P, int64_t C,
+                    int heads, int kv_heads, int dq, int dv, float scale, int num_splits,
+                    void* out, float* lse, void* workspace, size_t ws_bytes, cudaStream_t st) {
+  if (!q || !k_cache || !v_cache || !out) return VPP_ERR_INVALID;
+  if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
+  if (q_dtype != VPP_BF16 && q_dtype != VPP_FP32) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!supported_dims(dq, dv)) return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return VPP_ERR_INVALID;
+  if (P + C > (int64_t)INT32_MAX / 2 || C > (int64_t)INT32_MAX / 2) return VPP_ERR_INVALID;
+  if (block_table) {
+    if ((int64_t)num_blocks * kBlockTokens < P + C) return VPP_ERR_INVALID;
+  } else if ((int64_t)num_blocks < P + C) {
+    return VPP_ERR_INVALID;
+  }
+  if (C == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+
+  const SplitPlan sp = plan_splits(P, C, heads, kv_heads, dv, num_splits, ds->num_sms);
+  const size_t need_q = ws_q_bytes(q_dtype, C, heads, dq);
+  const size_t need_s = ws_split_bytes(sp.n_splits, C, heads, dv);
+  if (need_q + need_s > 0 && (!workspace || ws_bytes < need_q + need_s || !aligned16(workspace)))
+    return VPP_ERR_WORKSPACE;
+
+  const void* q_bf16 = q;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (q_dtype == VPP_FP32) {
+    if (launch_convert_f32_bf16(static_cast<const float*>(q), reinterpret_cast<uint16_t*>(ws),
+                                C * heads * dq, ds->num_sms, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+    q_bf16 = ws;
+  }
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (make_q_map(&tm_q, q_bf16, C, heads, kv_heads, dq)) return VPP_ERR_INVALID;
+  if (block_table) {
+    if (make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, dq) ||
+        make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, dv))
+      return VPP_ERR_INVALID;
+  } else {
+    if (make_contig_map(&tm_k, k_cache, P + C, kv_heads, dq) ||
+        make_contig_map(&tm_v, v_cache, P + C, kv_heads, dv))
+      return VPP_ERR_INVALID;
+  }
+
+  static AttnParams zero_params;  // value-initialised template
+  AttnParams p = zero_params;
+  p.n_segs = 1;
+  p.heads = heads;
+  p.kv_heads = kv_heads;
+  p.group = heads / kv_heads;
+  p.num_blocks = block_table ? num_blocks : 0;
+  p.paged = block_table ? 1 : 0;
+  p.scale_log2 = (scale > 0.f ? scale : 1.0f / std::sqrt((float)dq)) * 1.4426950408889634f;
+  p.block_table = block_table;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.lse_stride = C;
+  p.status = ds->status;
+  if (sp.n_splits > 1) {
+    p.ws_o = reinterpret_cast<float*>(ws + need_q);
+    p.ws_lse = reinterpret_cast<float*>(ws + need_q + round_up((size_t)sp.n_splits * C * heads * dv * 4, 256));
+  }
+  AttnSeg& s = p.segs[0];
+  s.q_start = 0;
+  s.q_len = (int32_t)C;
+  s.kv_len = (int32_t)(P + C);
+  s.table_off = 0;
+  s.n_pairs = pairs_for(C, p.group);
+  s.n_splits = sp.n_splits;
+  s.split_keys = sp.n_splits > 1 ? sp.split_keys : 0;
+  s.cta_begin = 0;
+  s.ws_row0 = 0;
+  const int64_t grid = (int64_t)s.n_pairs * kv_heads * s.n_splits;
+  if (grid > INT32_MAX) return VPP_ERR_INVALID;
+  if (launch_chunk_attn(dq, dv, tm_q, tm_k, tm_v, p, (int)grid, st) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  if (sp.n_splits > 1) {
+    if (launch_lse_merge(p.ws_o, p.ws_lse, 0, sp.n_splits, (int)C, 0, heads, dv,
+                         static_cast<uint16_t*>(out), lse, C, ds->num_sms, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+  }
+  return VPP_OK;
+}
+
+int build_varlen_plan(const int32_t* cu, const int32_t* ctx, int32_t batch, VarlenPlan* plan) {
+  if (!cu || !ctx || batch <= 0 || batch > kMaxBatch) return VPP_ERR_INVALID;
+  if (cu[0] != 0) return VPP_ERR_INVALID;
+  plan->batch = batch;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t ql = cu[b + 1] - cu[b];
+    if (ql < 0 || ctx[b] < ql || ctx[b] < 0) return VPP_ERR_INVALID;
+    plan->cu_q[b] = cu[b];
+    plan->ctx[b] = ctx[b];
+  }
+  plan->cu_q[batch] = cu[batch];
+  return VPP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vpp_status_string(int status) {
+  switch (status) {
+    case VPP_OK: return "VPP_OK";
+    case VPP_ERR_INVALID: return "VPP_ERR_INVALID: invalid argument";
+    case VPP_ERR_UNSUPPORTED: return "VPP_ERR_UNSUPPORTED: unsupported shape or device";
+    case VPP_ERR_CUDA: return "VPP_ERR_CUDA: a CUDA call failed";
+    case VPP_ERR_TIMEOUT: return "VPP_ERR_TIMEOUT: a device-side wait timed out";
+    case VPP_ERR_WORKSPACE: return "VPP_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown vpp status";
+  }
+}
+
+int vpp_version(void) { return 100; }
+
+int vpp_kv_append(const void* k_new, const void* v_new, int in_dtype, void* k_cache,
+                  void* v_cache, const int32_t* block_table, int32_t num_blocks,
+                  int64_t prefix_len, int64_t chunk_len, int kv_heads, int head_dim_qk,
+                  int head_dim_v, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache) return VPP_ERR_INVALID;
+  if (prefix_len < 0 || chunk_len < 0 || num_blocks <= 0 || kv_heads <= 0) return VPP_ERR_INVALID;
+  if (in_dtype != VPP_BF16 && in_dtype != VPP_FP32) return VPP_ERR_INVALID;
+  if (head_dim_qk <= 0 || head_dim_v <= 0 || head_dim_qk % 64 || head_dim_v % 64)
+    return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return VPP_ERR_INVALID;
+  const int64_t end = prefix_len + chunk_len;
+  if (block_table ? (int64_t)num_blocks * kBlockTokens < end : (int64_t)num_blocks < end)
+    return VPP_ERR_INVALID;
+  if (chunk_len == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  if (launch_kv_append(k_new, v_new, in_dtype == VPP_FP32, k_cache, v_cache, block_table,
+                       num_blocks, prefix_len, chunk_len, kv_heads, head_dim_qk, head_dim_v,
+                       ds->status, ds->num_sms, as_stream(stream)) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return VPP_OK;
+}
+
+int vpp_kv_append_varlen(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                         int32_t num_blocks, const int32_t* cu_seqlens_q,
+                         const int32_t* ctx_lens, int32_t batch, int kv_heads, int head_dim_qk,
+                         int head_dim_v, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table) return VPP_ERR_INVALID;
+  if (num_blocks <= 0 || kv_heads <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
+  if (head_dim_qk <= 0 || head_dim_v <= 0 || head_dim_qk % 64 || head_dim_v % 64)
+    return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return VPP_ERR_INVALID;
+  static VarlenPlan zero_plan;
+  VarlenPlan plan = zero_plan;
+  plan.max_blocks_per_seq = max_blocks_per_seq;
+  if (int r = build_varlen_plan(cu_seqlens_q, ctx_lens, batch, &plan)) return r;
+  for (int b = 0; b < batch; ++b)
+    if (ceil_div(ctx_lens[b], kBlockTokens) > max_blocks_per_seq) return VPP_ERR_INVALID;
+  if (plan.cu_q[batch] == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  if (launch_kv_append_varlen(k_new, v_new, k_cache, v_cache, block_table, plan, num_blocks,
+                              kv_heads, head_dim_qk, head_dim_v, ds->status, ds->num_sms,
+                              as_stream(stream)) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return VPP_OK;
+}
+
+int vpp_chunk_attn(const void* q, const void* k_cache, const void* v_cache, int64_t prefix_len,
+                   int64_t chunk_len, int heads, int kv_heads, int head_dim, void* out,
+                   float* lse, void* stream) {
+  if (prefix_len < 0 || chunk_len < 0) return VPP_ERR_INVALID;
+  const int64_t cap = prefix_len + chunk_len;
+  if (cap > INT32_MAX) return VPP_ERR_INVALID;
+  return chunk_attn_impl(q, VPP_BF16, k_cache, v_cache, nullptr, (int32_t)std::max<int64_t>(cap, 1),
+                         prefix_len, chunk_len, heads, kv_heads, head_dim, head_dim, 0.f, 1, out,
+                         lse, nullptr, 0, as_stream(stream));
+}
+
+int vpp_chunk_attn_ex(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, int32_t num_blocks, int64_t prefix_len,
+                      int64_t chunk_len, int heads, int kv_heads, int head_dim_qk,
+                      int head_dim_v, float softmax_scale, int num_splits, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return chunk_attn_impl(q, q_dtype, k_cache, v_cache, block_table, num_blocks, prefix_len,
+                         chunk_len, heads, kv_heads, head_dim_qk, head_dim_v, softmax_scale,
+                         num_splits, out, lse, workspace, workspace_bytes, as_stream(stream));
+}
+
+int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
+                              int head_dim_qk, int head_dim_v, int num_splits) {
+  if (prefix_len < 0 || chunk_len < 0 || num_splits < 0) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
+  DeviceState* ds = nullptr;
+  int num_sms = 152;
+  if (device_state(&ds) == VPP_OK) num_sms = ds->num_sms;
+  return plan_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_v, num_splits, num_sms)
+      .n_splits;
+}
+
+size_t vpp_chunk_attn_workspace_size(int q_dtype, int64_t prefix_len, int64_t chunk_len,
+                                     int heads, int kv_heads, int head_dim_qk, int head_dim_v,
+                                     int num_splits) {
+  const int S = vpp_chunk_attn_num_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
+                                          head_dim_v, num_splits);
+  if (S < 1) return 0;
+  return ws_q_bytes(q_dtype, chunk_len, heads, head_dim_qk) +
+         ws_split_bytes(S, chunk_len, heads, head_dim_v);
+}
+
+int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                   const int32_t* cu_seqlens_q, const int32_t* ctx_lens, int32_t batch,
+                   int heads, int kv_heads, int head_dim_qk, int head_dim_v,
+                   float softmax_scale, void* out, float* lse, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!q || !k_cache || !v_cache || !block_table || !out) return VPP_ERR_INVALID;
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return VPP_ERR_INVALID;
+  static VarlenPlan zero_plan;
+  VarlenPlan plan = zero_plan;
+  if (int r = build_varlen_plan(cu_seqlens_q, ctx_lens, batch, &plan)) return r;
+  for (int b = 0; b < batch; ++b)
+    if (ceil_div(ctx_lens[b], kBlockTokens) > max_blocks_per_seq) return VPP_ERR_INVALID;
+  const int64_t total_q = cu_seqlens_q[batch];
+  if (total_q == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  cudaStream_t st = as_stream(stream);
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (make_q_map(&tm_q, q, total_q, heads, kv_heads, head_dim_qk) ||
+      make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
+      make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v))
+    return VPP_ERR_INVALID;
+
+  static AttnParams zero_params;
+  AttnParams p = zero_params;
+  p.heads = heads;
+  p.kv_heads = kv_heads;
+  p.group = heads / kv_heads;
+  p.num_blocks = num_blocks;
+  p.paged = 1;
+  p.scale_log2 =
+      (softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)head_dim_qk)) * 1.4426950408889634f;
+  p.block_table = block_table;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.lse_stride = total_q;
+  p.status = ds->status;
+
+  // Every sequence with queries becomes one segment; segments are ordered by
+  // per-CTA work (keys per CTA) so the heaviest CTAs start first.
+  int order[kMaxBatch];
+  int n = 0;
+  for (int b = 0; b < batch; ++b)
+    if (cu_seqlens_q[b + 1] > cu_seqlens_q[b]) order[n++] = b;
+  std::stable_sort(order, order + n, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
+  for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
+    const int cnt = std::min(kMaxAttnSegs, n - i0);
+    int64_t cta = 0;
+    p.n_segs = cnt;
+    for (int i = 0; i < cnt; ++i) {
+      const int b = order[i0 + i];
+      AttnSeg& s = p.segs[i];
+      s.q_start = cu_seqlens_q[b];
+      s.q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+      s.kv_len = ctx_lens[b];
+      s.table_off = b * max_blocks_per_seq;
+      s.n_pairs = pairs_for(s.q_len, p.group);
+      s.n_splits = 1;
+      s.split_keys = 0;
+      s.cta_begin = (int32_t)cta;
+      s.ws_row0 = 0;
+      cta += (int64_t)s.n_pairs * kv_heads;
+    }
+    if (cta > INT32_MAX) return VPP_ERR_INVALID;
+    if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) !=
+        cudaSuccess)
+      return VPP_ERR_CUDA;
+  }
+  return VPP_OK;
+}
+
+size_t vpp_mixed_attn_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                     int32_t batch, int heads, int kv_heads, int head_dim_qk,
+                                     int head_dim_v) {
+  (void)cu_seqlens_q;
+  (void)ctx_lens;
+  (void)batch;
+  (void)heads;
+  (void)kv_heads;
+  (void)head_dim_qk;
+  (void)head_dim_v;
+  return 0;
+}
+
+int vpp_last_device_status(void* stream, int* code) {
+  if (!code) return VPP_ERR_INVALID;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  cudaStream_t st = as_stream(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, ds->status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(ds->status, 0, sizeof(int), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  *code = host;
+  return VPP_OK;
+}
+
+int vpp_selftest_wait_timeout(int timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 5000000) return VPP_ERR_INVALID;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  if (launch_wait_timeout_selftest(timeout_us, ds->status, as_stream(stream)) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return VPP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// chunk_attn.cuh -- parameters of the chunk-attention kernel (shared with api.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace vpp {
+
+constexpr int kTileM = 128;        // query rows per tile (tokens x GQA heads)
+constexpr int kTileN = 128;        // keys per KV tile
+constexpr int kMaxAttnSegs = 64;   // prefill segments per launch
+
+// One prefill segment: a chunk of one sequence (a7 splits its key range).
+struct AttnSeg {
+  int32_t q_start;     // first packed query row (token) of the segment in q/out
+  int32_t q_len;       // C
+  int32_t kv_len;      // P + C keys in the cache
+  int32_t table_off;   // offset (entries) of the sequence's block-table row
+  int32_t n_pairs;     // CTAs per (kv head, split): pairs of query tiles
+  int32_t n_splits;    // key ranges (1 = write the final output directly)
+  int32_t split_keys;  // keys per non-final range, multiple of kTileN
+  int32_t cta_begin;   // first CTA index of this segment
+  int64_t ws_row0;     // first workspace row of this segment's partials
+};
+
+struct AttnParams {
+  int32_t n_segs;
+  int32_t heads;
+  int32_t kv_heads;
+  int32_t group;          // heads / kv_heads
+  int32_t num_blocks;     // paged: blocks in the pool (an out-of-range block reads zeros)
+  int32_t paged;          // 1: 4-D paged K/V maps, 0: 3-D contiguous maps
+  float scale_log2;       // softmax scale * log2(e)
+  int32_t pad0;
+  const int32_t* block_table;
+  uint16_t* out;          // bf16 [total_q][heads][dv]
+  float* lse;             // [heads][lse_stride] float32, may be null
+  int64_t lse_stride;
+  float* ws_o;            // split partials, float32 [rows][heads][dv]
+  float* ws_lse;          // [rows][heads]
+  int* status;
+  AttnSeg segs[kMaxAttnSegs];
+};
+
+// Smem and thread shape of one instantiation.
+constexpr int kAttnThreads = 384;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, WG1/WG2 softmax
+constexpr int kSmemLimit = 232448; // 227 KB per CTA on sm_103a
+constexpr int kSubTileBytes = kTileN * 64 * 2;  // 128 keys x 64 bf16 (one 128B-swizzled block)
+
+__host__ __device__ constexpr int attn_q_bytes(int dq) { return 2 * (dq / 64) * kSubTileBytes; }
+__host__ __device__ constexpr int attn_num_slots(int dq) {
+  return (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes > 12
+             ? 12
+             : (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes;
+}
+__host__ __device__ constexpr int attn_smem_bytes(int dq) {
+  return 1024 + attn_q_bytes(dq) + attn_num_slots(dq) * kSubTileBytes + 1024;
+}
+
+cudaError_t launch_chunk_attn(int dq, int dv, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                              cudaStream_t stream);
+
+// Merge of split partials for one segment (a7).
+cudaError_t launch_lse_merge(const float* ws_o, const float* ws_lse, int64_t ws_row0,
+                             int n_splits, int q_len, int q_start, int heads, int dv,
+                             uint16_t* out, float* lse, int64_t lse_stride, int num_sms,
+                             cudaStream_t stream);
+
+}  // namespace vpp

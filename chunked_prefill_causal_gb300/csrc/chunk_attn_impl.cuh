@@ -1,0 +1,468 @@
+// chunk_attn_impl.cuh -- a2..a6: causal attention of one prefill chunk (or of
+// several prefill segments of a mixed batch) over its cached prefix plus
+// itself, on tcgen05 tensor cores.
+//
+// Method: Eq. (1) of "VPP: Virtual Pipeline Parallelism for Efficient Chunked
+// Prefill in Long-Context LLM Inference" (technical review, §2.2),
+// softmax(Q K^T / sqrt(d)) V, with token i attending to tokens <= i, for a
+// chunk whose first token sits at absolute position P = kv_len - q_len (§2.3:
+// a later chunk attends to the whole cached prefix plus itself).  The softmax
+// is evaluated online over 128-key tiles (running max m and denominator l per
+// row, exact after the final division); the result and ln(denominator) are
+// written, or, when the key range is split, float32 partials and their LSE for
+// the merge kernel ("02 · 并行策略与 PP 切分" note, §7: partial results over
+// disjoint key ranges are combined through their LSE).
+//
+// CTA shape (384 threads, one CTA per SM):
+//   warp 0      TMA producer: the CTA's two 128-row query tiles once, then K
+//               and V tiles as 16 KB sub-tiles (128 keys x 64 dims) through a
+//               ring of shared-memory slots (full/empty mbarrier pairs).
+//   warp 1      MMA issuer (one elected lane): S = Q K^T into TMEM (kind::f16,
+//               bf16 in, f32 accumulate), then O += P V with P read from TMEM.
+//   warp 2      allocates and frees the 512 TMEM columns.
+//   warps 4-7   softmax + epilogue of query tile A; warps 8-11 of tile B.
+//               Each thread owns one query row = one TMEM lane, so row max and
+//               row sum need no shuffles.
+// TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+DV) O_B [256+DV,256+2DV).
+// P (bf16 pairs) overwrites the first 64 columns of its S tile.
+//
+// Query rows: a 128-row tile holds 128/G consecutive tokens x the G query
+// heads of one kv head (GQA packing), so every K/V tile loaded serves all
+// 2 x 128 rows of the CTA.  The causal mask is applied only on tiles that
+// reach past a row's position; prefix tiles are never masked.
+//
+// The MMA issue order per KV tile j is PV(A,j), QK(A,j+1), PV(B,j), QK(B,j+1):
+// while one softmax group works on its S tile the tensor core runs the other
+// tile's PV and QK.  Every mbarrier wait is bounded; a timeout records
+// VPP_ERR_TIMEOUT in the status word and every role leaves its loop.
+#pragma once
+
+#include "chunk_attn.cuh"
+#include "ptx.cuh"
+
+namespace vpp {
+namespace attn_detail {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
+
+struct Ring {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ void advance(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+template <int DQ, int DV>
+struct Shape {
+  static constexpr int NQC = DQ / 64;  // 64-dim sub-tiles of a K tile (and of Q)
+  static constexpr int NVC = DV / 64;  // 64-dim sub-tiles of a V tile
+  static constexpr int NSLOT = attn_num_slots(DQ);
+  static constexpr int QBYTES = attn_q_bytes(DQ);
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kTileN, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, 64, false, true);
+  // barrier indices
+  static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_FULL = 8,
+                       B_EMPTY = 8 + NSLOT, NBARS = 8 + 2 * NSLOT;
+  static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
+  static_assert(DV <= 128, "O accumulators must fit TMEM next to two S tiles");
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status,
+                                          volatile uint32_t* abort) {
+  const bool ok = mbar_wait(bar, parity, status, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace attn_detail
+
+template <int DQ, int DV>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    chunk_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ AttnParams p) {
+  using namespace attn_detail;
+  using S = Shape<DQ, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + S::QBYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSLOT * kSubTileBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------- work item
+  int si = 0;
+  while (si + 1 < p.n_segs && p.segs[si + 1].cta_begin <= static_cast<int>(blockIdx.x)) ++si;
+  const AttnSeg& seg = p.segs[si];
+  const int local = static_cast<int>(blockIdx.x) - seg.cta_begin;
+  const int split = local % seg.n_splits;
+  const int rest = local / seg.n_splits;
+  const int g = rest % p.kv_heads;
+  const int pair = seg.n_pairs - 1 - rest / p.kv_heads;  // heaviest pairs first
+  const int G = p.group;
+  const int T = kTileM / G;      // tokens per query tile
+  const int tok0 = pair * 2 * T;  // first token of tile A (segment-relative)
+  const int P = seg.kv_len - seg.q_len;
+  const int k_lo = split * seg.split_keys;
+  const int k_hi = (split == seg.n_splits - 1) ? P + min(tok0 + 2 * T, seg.q_len)
+                                               : (split + 1) * seg.split_keys;
+  const int n_kv = (k_hi - k_lo + kTileN - 1) / kTileN;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bar(S::B_Q), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(S::B_S + x), 1);
+      mbar_init(bar(S::B_P + x), 128);
+      mbar_init(bar(S::B_O + x), 1);
+    }
+    mbar_init(bar(S::B_FINAL), 1);
+    for (int i = 0; i < S::NSLOT; ++i) {
+      mbar_init(bar(S::B_FULL + i), 1);
+      mbar_init(bar(S::B_EMPTY + i), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(S::B_Q), 2 * S::NQC * kSubTileBytes);
+      for (int x = 0; x < 2; ++x)
+        for (int c = 0; c < S::NQC; ++c)
+          tma_load_4d(smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes), &tm_q, bar(S::B_Q),
+                      c * 64, 0, g, seg.q_start + tok0 + x * T);
+      Ring r{0, 0u};
+      uint32_t filled = 0u, fill_phase = 0u;
+      bool ok = true;
+      auto block_coord = [&](int b) -> int {
+        if (b * kBlockTokens >= seg.kv_len) return p.num_blocks;  // reads zeros
+        const int e = p.block_table[seg.table_off + b];
+        if (e < 0 || e >= p.num_blocks) {
+          record_status(p.status, kStatusInvalid);
+          return p.num_blocks;
+        }
+        return e;
+      };
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int key0 = k_lo + j * kTileN;
+        int c0, c1;
+        if (p.paged) {
+          c0 = block_coord(key0 / kBlockTokens);
+          c1 = block_coord(key0 / kBlockTokens + 1);
+        } else {
+          c0 = key0;
+          c1 = key0 + kBlockTokens;
+        }
+        for (int c = 0; c < S::NQC + S::NVC; ++c) {
+          if (!mbar_wait(bar(S::B_EMPTY + r.slot), r.phase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = smem_u32(sRing + r.slot * kSubTileBytes);
+          const uint32_t fb = bar(S::B_FULL + r.slot);
+          mbar_arrive_expect_tx(fb, kSubTileBytes);
+          const CUtensorMap* m = c < S::NQC ? &tm_k : &tm_v;
+          const int dc = (c < S::NQC ? c : c - S::NQC) * 64;
+          if (p.paged) {
+            tma_load_4d(dst, m, fb, dc, g, 0, c0);
+            tma_load_4d(dst + kSubTileBytes / 2, m, fb, dc, g, 0, c1);
+          } else {
+            tma_load_3d(dst, m, fb, dc, g, c0);
+            tma_load_3d(dst + kSubTileBytes / 2, m, fb, dc, g, c1);
+          }
+          filled |= 1u << r.slot;
+          fill_phase = (fill_phase & ~(1u << r.slot)) | (r.phase << r.slot);
+          r.advance(S::NSLOT);
+        }
+      }
+      if (!ok) {
+        // Let every copy this thread started land before the CTA exits.
+        for (int i = 0; i < S::NSLOT; ++i)
+          if (filled & (1u << i))
+            mbar_wait_for(bar(S::B_FULL + i), (fill_phase >> i) & 1u, 100000000ull);
+        mbar_wait_for(bar(S::B_Q), 0, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    Ring r{0, 0u};
+    auto qk = [&](int x, int kslot) {
+      const uint32_t d = tbase + x * kTileN;
+#pragma unroll
+      for (int c = 0; c < S::NQC; ++c) {
+        const uint32_t qa = smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes);
+        const uint32_t kb = smem_u32(sRing + ((kslot + c) % S::NSLOT) * kSubTileBytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(d, sdesc_sw128(qa + 32 * k, 16, 1024), sdesc_sw128(kb + 32 * k, 16, 1024),
+                  S::IDESC_QK, (c | k) ? 1u : 0u);
+      }
+    };
+    auto pv = [&](int x, int vslot, bool acc) {
+      const uint32_t a = tbase + x * kTileN;
+#pragma unroll
+      for (int h = 0; h < S::NVC; ++h) {
+        const uint32_t d = tbase + 2 * kTileN + x * DV + h * 64;
+        const uint32_t vb = smem_u32(sRing + ((vslot + h) % S::NSLOT) * kSubTileBytes);
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k)
+          umma_ts(d, a + 8 * k, sdesc_sw128(vb + 2048 * k, 16384, 1024), S::IDESC_PV,
+                  (acc || k) ? 1u : 0u);
+      }
+    };
+    auto wait_slots = [&](int n) -> bool {
+      for (int c = 0; c < n; ++c) {
+        if (!warp_wait(bar(S::B_FULL + r.slot), r.phase, p.status, abort_flag)) return false;
+        r.advance(S::NSLOT);
+      }
+      return true;
+    };
+    bool ok = warp_wait(bar(S::B_Q), 0, p.status, abort_flag);
+    if (ok) {
+      const int kslot = r.slot;
+      ok = wait_slots(S::NQC);
+      if (ok) {
+        tc_fence_after();
+        if (lane == 0) {
+          qk(0, kslot);
+          umma_commit(bar(S::B_S + 0));
+          qk(1, kslot);
+          umma_commit(bar(S::B_S + 1));
+          for (int c = 0; c < S::NQC; ++c) umma_commit(bar(S::B_EMPTY + (kslot + c) % S::NSLOT));
+        }
+        __syncwarp();
+      }
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int vslot = r.slot;
+      if (!(ok = wait_slots(S::NVC))) break;
+      if (p.paged && j == n_kv - 1) {
+        // Rows of the last loaded block at positions >= kv_len hold whatever
+        // the pool holds there; zero their V rows so that P = 0 times them
+        // stays 0 (K rows there are masked to -inf before the softmax).
+        const int key0 = k_lo + j * kTileN;
+        const int r0 = seg.kv_len - key0;
+        if (r0 > 0 && r0 < kTileN && (r0 % kBlockTokens) != 0) {
+          const int r1 = (r0 + kBlockTokens - 1) / kBlockTokens * kBlockTokens;
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int h = 0; h < S::NVC; ++h) {
+            uint8_t* base = sRing + ((vslot + h) % S::NSLOT) * kSubTileBytes;
+            for (int idx = lane; idx < (r1 - r0) * 8; idx += 32)
+              *reinterpret_cast<uint4*>(base + (r0 + idx / 8) * 128 + (idx % 8) * 16) = z;
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+      }
+      if (!(ok = warp_wait(bar(S::B_P + 0), j & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        pv(0, vslot, j > 0);
+        if (j == n_kv - 1) umma_commit(bar(S::B_O + 0));
+      }
+      __syncwarp();
+      int nk = -1;
+      if (j + 1 < n_kv) {
+        nk = r.slot;
+        if (!(ok = wait_slots(S::NQC))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          qk(0, nk);
+          umma_commit(bar(S::B_S + 0));
+        }
+        __syncwarp();
+      }
+      if (!(ok = warp_wait(bar(S::B_P + 1), j & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        pv(1, vslot, j > 0);
+        for (int h = 0; h < S::NVC; ++h) umma_commit(bar(S::B_EMPTY + (vslot + h) % S::NSLOT));
+        if (j == n_kv - 1) umma_commit(bar(S::B_O + 1));
+        if (nk >= 0) {
+          qk(1, nk);
+          umma_commit(bar(S::B_S + 1));
+          for (int c = 0; c < S::NQC; ++c) umma_commit(bar(S::B_EMPTY + (nk + c) % S::NSLOT));
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // Every MMA issued so far must finish before TMEM is freed.
+      umma_commit(bar(S::B_FINAL));
+      mbar_wait_for(bar(S::B_FINAL), 0, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ softmax + epilogue
+    const int x = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int tok = tok0 + x * T + row / G;
+    const int hq = g * G + row % G;
+    const int lim = min(P + tok, seg.kv_len - 1);  // last visible key (inclusive)
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + x * kTileN;
+    const uint32_t tO = lane_base + 2 * kTileN + x * DV;
+    const float sl = p.scale_log2;
+    float m = -INFINITY;  // running max of score * scale * log2(e)
+    float l = 0.f;        // running denominator, relative to 2^m
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = warp_wait(bar(S::B_S + x), j & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      uint32_t u[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32 * q, u[q]);
+      tmem_ld_wait();
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(u[c >> 5][c & 31]);
+      const int key0 = k_lo + j * kTileN;
+      if (key0 + kTileN - 1 > lim) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (key0 + c > lim) sv[c] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_new = fmaxf(m, mx * sl);
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O of this tile is idle here: PV(x, j-1) completed before S(x, j)
+          // was committed, and PV(x, j) waits for this group's P.
+          const float f = need ? ex2_approx(m - m_new) : 1.f;
+          if (need) {
+            l *= f;
+            m = m_new;
+          }
+#pragma unroll
+          for (int q = 0; q < DV / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * q, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(tO + 32 * q, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float a = ex2_approx(fmaf(sv[2 * c], sl, -mb));
+        const float b = ex2_approx(fmaf(sv[2 * c + 1], sl, -mb));
+        rs += a + b;
+        pk[c >> 5][c & 31] = pack_bf16x2(a, b);
+      }
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(S::B_P + x));
+      l += rs;
+    }
+    if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = tok < seg.q_len;
+      const float inv = 1.f / l;
+      const float lse_v = m * kLn2 + logf(l);
+      if (seg.n_splits == 1) {
+        uint16_t* orow = p.out + (static_cast<int64_t>(seg.q_start + tok) * p.heads + hq) * DV;
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * q, o);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (valid && p.lse) p.lse[static_cast<int64_t>(hq) * p.lse_stride + seg.q_start + tok] = lse_v;
+      } else {
+        const int64_t wrow = seg.ws_row0 + static_cast<int64_t>(split) * seg.q_len + tok;
+        float* orow = p.ws_o + (wrow * p.heads + hq) * DV;
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * q, o);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(orow + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                   __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+          }
+        }
+        if (valid) p.ws_lse[wrow * p.heads + hq] = lse_v;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int DQ, int DV>
+cudaError_t launch_chunk_attn_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                                cudaStream_t stream) {
+  constexpr int smem = attn_smem_bytes(DQ);
+  static_assert(smem <= kSmemLimit, "shared memory budget");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(chunk_attn_kernel<DQ, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  chunk_attn_kernel<DQ, DV><<<grid, kAttnThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace vpp

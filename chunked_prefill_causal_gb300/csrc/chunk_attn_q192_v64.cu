@@ -1,0 +1,8 @@
+// Instantiation of the chunk-attention kernel for head_dim_qk = 192, head_dim_v = 64.
+#include "chunk_attn_impl.cuh"
+
+namespace vpp {
+template cudaError_t launch_chunk_attn_t<192, 64>(const CUtensorMap&, const CUtensorMap&,
+                                                const CUtensorMap&, const AttnParams&, int,
+                                                cudaStream_t);
+}  // namespace vpp

@@ -1,0 +1,86 @@
+"""The C ABI library loads, exports every symbol include/vpp.h declares, and
+rejects bad arguments on the host before touching a device (runs on CPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunked_prefill_causal_gb300 import vpp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vpp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return vpp.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vpp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("vpp_kv_append", "vpp_chunk_attn", "vpp_chunk_attn_ex", "vpp_mixed_attn",
+              "vpp_last_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_symbols()) <= set(vpp.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert vpp.status_string(code)
+    assert "unknown" in vpp.status_string(42)
+    assert lib.vpp_version() >= 100
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    null = None
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    # null tensors
+    assert lib.vpp_chunk_attn(null, fake, fake, 0, 16, 8, 2, 128, fake, null, null) == vpp.VPP_ERR_INVALID
+    # unsupported head dim / grouping
+    assert lib.vpp_chunk_attn(fake, fake, fake, 0, 16, 8, 2, 96, fake, null, null) == vpp.VPP_ERR_UNSUPPORTED
+    assert lib.vpp_chunk_attn(fake, fake, fake, 0, 16, 24, 8, 128, fake, null, null) == vpp.VPP_ERR_UNSUPPORTED
+    assert lib.vpp_chunk_attn(fake, fake, fake, 0, 16, 7, 2, 128, fake, null, null) == vpp.VPP_ERR_INVALID
+    # misaligned pointer
+    bad = ctypes.c_void_p(0x100004)
+    assert lib.vpp_chunk_attn(bad, fake, fake, 0, 16, 8, 2, 128, fake, null, null) == vpp.VPP_ERR_INVALID
+    # negative lengths
+    assert lib.vpp_chunk_attn(fake, fake, fake, -1, 16, 8, 2, 128, fake, null, null) == vpp.VPP_ERR_INVALID
+    # cache too small for prefix + chunk (paged: 2 blocks = 128 tokens)
+    assert lib.vpp_chunk_attn_ex(fake, 0, fake, fake, fake, 2, 100, 29, 8, 2, 128, 128, 0.0, 0, fake,
+                                 null, null, 0, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_kv_append(fake, fake, 0, fake, fake, fake, 2, 100, 29, 2, 128, 128, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_kv_append(fake, fake, 7, fake, fake, fake, 2, 0, 29, 2, 128, 128, null) == vpp.VPP_ERR_INVALID
+    # varlen: cu_seqlens must start at 0 and ctx >= q_len
+    cu = (ctypes.c_int32 * 3)(0, 5, 9)
+    ctx = (ctypes.c_int32 * 2)(4, 10)
+    assert lib.vpp_mixed_attn(fake, fake, fake, fake, 4, 16, cu, ctx, 2, 8, 2, 128, 128, 0.0, fake, null,
+                              null, 0, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_selftest_wait_timeout(0, null) == vpp.VPP_ERR_INVALID
+
+
+def test_split_plan_is_host_side(lib):
+    # No device needed: the planner falls back to 152 SMs for its model.
+    assert vpp.chunk_attn_num_splits(0, 4096, 32, 8, 128, 128) == 1
+    assert vpp.chunk_attn_num_splits(7 * 16384, 16384, 64, 8, 128, 128) == 1
+    assert vpp.chunk_attn_num_splits(100000, 64, 8, 8, 128, 128, num_splits=4) == 4
+    assert vpp.chunk_attn_num_splits(300, 64, 8, 8, 128, 128, num_splits=8) <= 3
+    assert vpp.chunk_attn_num_splits(100000, 64, 8, 8, 128, 128, num_splits=1) == 1
+    ws = vpp.chunk_attn_workspace_size(vpp.VPP_BF16, 100000, 64, 8, 8, 128, 128, 4)
+    assert ws >= 4 * 64 * 8 * 128 * 4
+    assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, 100000, 64, 8, 8, 128, 128, 1) == 0
+    assert vpp.chunk_attn_workspace_size(vpp.VPP_FP32, 0, 64, 8, 8, 128, 128, 1) == 64 * 8 * 128 * 2
