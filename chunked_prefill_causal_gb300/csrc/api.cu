@@ -178,8 +178,9 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
                     const int32_t* block_table, int32_t num_blocks, int64_t P, int64_t C,
                     int heads, int kv_heads, int dq, int dv, float scale, int num_splits,
                     void* out, float* lse, void* workspace, size_t ws_bytes, cudaStream_t st) {
-  if (!q || !k_cache || !v_cache || !out) return VPP_ERR_INVALID;
   if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
+  if (C == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
+  if (!q || !k_cache || !v_cache || !out) return VPP_ERR_INVALID;
   if (q_dtype != VPP_BF16 && q_dtype != VPP_FP32) return VPP_ERR_INVALID;
   if (int r = check_heads(heads, kv_heads)) return r;
   if (!supported_dims(dq, dv)) return VPP_ERR_UNSUPPORTED;
@@ -299,8 +300,9 @@ int vpp_kv_append(const void* k_new, const void* v_new, int in_dtype, void* k_ca
                   void* v_cache, const int32_t* block_table, int32_t num_blocks,
                   int64_t prefix_len, int64_t chunk_len, int kv_heads, int head_dim_qk,
                   int head_dim_v, void* stream) {
-  if (!k_new || !v_new || !k_cache || !v_cache) return VPP_ERR_INVALID;
   if (prefix_len < 0 || chunk_len < 0 || num_blocks <= 0 || kv_heads <= 0) return VPP_ERR_INVALID;
+  if (chunk_len == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
+  if (!k_new || !v_new || !k_cache || !v_cache) return VPP_ERR_INVALID;
   if (in_dtype != VPP_BF16 && in_dtype != VPP_FP32) return VPP_ERR_INVALID;
   if (head_dim_qk <= 0 || head_dim_v <= 0 || head_dim_qk % 64 || head_dim_v % 64)
     return VPP_ERR_UNSUPPORTED;

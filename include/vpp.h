@@ -94,7 +94,7 @@ int vpp_version(void);
  * layout, where num_blocks is instead the capacity in tokens.
  * Block-table entries are not read on the host; out-of-range entries are
  * skipped on the device and recorded as VPP_ERR_INVALID in the status word.
- * chunk_len == 0 is a no-op returning VPP_OK.
+ * chunk_len == 0 is a no-op returning VPP_OK (pointers may then be NULL).
  */
 int vpp_kv_append(const void *k_new, const void *v_new, int in_dtype,
                   void *k_cache, void *v_cache, const int32_t *block_table,
@@ -110,7 +110,7 @@ int vpp_kv_append(const void *k_new, const void *v_new, int in_dtype,
  * bf16 and lse [heads][chunk_len] float32 (lse may be NULL).  Query i
  * attends keys 0 .. prefix_len + i of the cache ([VPP review] §2.2 Eq. (1),
  * §2.3).  The chunk's own K/V must already be in the cache (vpp_kv_append
- * first).  chunk_len == 0 is a no-op.
+ * first).  chunk_len == 0 is a no-op (pointers may then be NULL).
  */
 int vpp_chunk_attn(const void *q, const void *k_cache, const void *v_cache,
                    int64_t prefix_len, int64_t chunk_len, int heads,
