@@ -15,10 +15,14 @@
 //
 // CTA shape (384 threads, one CTA per SM):
 //   warp 0      TMA producer: the CTA's two 128-row query tiles once, then K
-//               and V tiles as 16 KB sub-tiles (128 keys x 64 dims) through a
-//               ring of shared-memory slots (full/empty mbarrier pairs).
-//   warp 1      MMA issuer (one elected lane): S = Q K^T into TMEM (kind::f16,
-//               bf16 in, f32 accumulate), then O += P V with P read from TMEM.
+//               and V tiles through a ring of shared-memory stages (one stage
+//               = one K tile or one V tile, one full/empty mbarrier pair).
+//   warp 1, 3   MMA issuers, one elected lane each: warp 1 for query tile A,
+//               warp 3 for tile B.  S = Q K^T into TMEM (kind::f16, bf16 in,
+//               f32 accumulate), then O += P V with P read from TMEM.  Two
+//               issuers let one tile's MMAs run while the other waits for its
+//               softmax: a wait, commit or fence between MMA batches in the
+//               issuing thread leaves the tensor core idle otherwise.
 //   warp 2      allocates and frees the 512 TMEM columns.
 //   warps 4-7   softmax + epilogue of query tile A; warps 8-11 of tile B.
 //               Each thread owns one query row = one TMEM lane, so row max and
@@ -31,10 +35,8 @@
 // 2 x 128 rows of the CTA.  The causal mask is applied only on tiles that
 // reach past a row's position; prefix tiles are never masked.
 //
-// The MMA issue order per KV tile j is PV(A,j), QK(A,j+1), PV(B,j), QK(B,j+1):
-// while one softmax group works on its S tile the tensor core runs the other
-// tile's PV and QK.  Every mbarrier wait is bounded; a timeout records
-// VPP_ERR_TIMEOUT in the status word and every role leaves its loop.
+// Every mbarrier wait is bounded; a timeout records VPP_ERR_TIMEOUT in the
+// status word and every role leaves its loop.
 #pragma once
 
 #include "chunk_attn.cuh"
@@ -45,6 +47,10 @@ namespace attn_detail {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
+constexpr int kRegsLow = 72;
+constexpr int kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch");
+constexpr uint64_t kCleanupNs = 100000000ull;  // 0.1 s for clean-up waits after an abort
 
 struct Ring {
   int slot;
@@ -61,14 +67,15 @@ template <int DQ, int DV>
 struct Shape {
   static constexpr int NQC = DQ / 64;  // 64-dim sub-tiles of a K tile (and of Q)
   static constexpr int NVC = DV / 64;  // 64-dim sub-tiles of a V tile
-  static constexpr int NSLOT = attn_num_slots(DQ);
+  static constexpr int NSTAGE = attn_num_stages(DQ, DV);
+  static constexpr int STAGE_BYTES = attn_stage_bytes(DQ, DV);
   static constexpr int QBYTES = attn_q_bytes(DQ);
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kTileN, false, false);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, 64, false, true);
-  // barrier indices
-  static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_FULL = 8,
-                       B_EMPTY = 8 + NSLOT, NBARS = 8 + 2 * NSLOT;
-  static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, DV, false, true);
+  // barrier indices: Q, S[2], P[2], O[2], FINAL[2], TMP, FULL[NSTAGE], EMPTY[NSTAGE]
+  static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_FULL = 10,
+                       B_EMPTY = 10 + NSTAGE, NBARS = 10 + 2 * NSTAGE;
+  static_assert(NSTAGE >= 2, "ring must hold one K and one V tile");
   static_assert(DV <= 128, "O accumulators must fit TMEM next to two S tiles");
 };
 
@@ -93,7 +100,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + S::QBYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSLOT * kSubTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSTAGE * S::STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int g = rest % p.kv_heads;
   const int pair = seg.n_pairs - 1 - rest / p.kv_heads;  // heaviest pairs first
   const int G = p.group;
-  const int T = kTileM / G;      // tokens per query tile
+  const int T = kTileM / G;       // tokens per query tile
   const int tok0 = pair * 2 * T;  // first token of tile A (segment-relative)
   const int P = seg.kv_len - seg.q_len;
   const int k_lo = split * seg.split_keys;
@@ -126,11 +133,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(S::B_S + x), 1);
       mbar_init(bar(S::B_P + x), 128);
       mbar_init(bar(S::B_O + x), 1);
+      mbar_init(bar(S::B_FINAL + x), 1);
     }
-    mbar_init(bar(S::B_FINAL), 1);
-    for (int i = 0; i < S::NSLOT; ++i) {
+    mbar_init(bar(S::B_TMP), 1);
+    for (int i = 0; i < S::NSTAGE; ++i) {
       mbar_init(bar(S::B_FULL + i), 1);
-      mbar_init(bar(S::B_EMPTY + i), 1);
+      mbar_init(bar(S::B_EMPTY + i), 2);  // released by both MMA issuers
     }
     fence_mbar_init();
   }
@@ -143,9 +151,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  // Registers: the TMA/MMA/TMEM warpgroup needs few, the softmax warpgroups
+  // hold a 128-float score row each: 384 threads x 168 at launch >=
+  // 128 x kRegsLow + 256 x kRegsHigh.  Each branch starts with its own
+  // setmaxnreg so that the code it dominates is compiled for that budget.
+  if (warp < 4) {
+    regs_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -166,6 +179,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return e;
       };
+      // Loads nsub sub-tiles (two 64-key blocks each) of K or V into a stage.
+      auto load_part = [&](const CUtensorMap* m, int nsub, uint32_t dst, uint32_t fb, int c0,
+                           int c1) {
+        for (int c = 0; c < nsub; ++c) {
+          const uint32_t d = dst + c * kSubTileBytes;
+          if (p.paged) {
+            tma_load_4d(d, m, fb, c * 64, g, 0, c0);
+            tma_load_4d(d + kSubTileBytes / 2, m, fb, c * 64, g, 0, c1);
+          } else {
+            tma_load_3d(d, m, fb, c * 64, g, c0);
+            tma_load_3d(d + kSubTileBytes / 2, m, fb, c * 64, g, c1);
+          }
+        }
+      };
       for (int j = 0; ok && j < n_kv; ++j) {
         const int key0 = k_lo + j * kTileN;
         int c0, c1;
@@ -176,146 +203,109 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c0 = key0;
           c1 = key0 + kBlockTokens;
         }
-        for (int c = 0; c < S::NQC + S::NVC; ++c) {
+        for (int part = 0; part < 2; ++part) {  // K, then V
           if (!mbar_wait(bar(S::B_EMPTY + r.slot), r.phase ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t dst = smem_u32(sRing + r.slot * kSubTileBytes);
+          const uint32_t dst = smem_u32(sRing + r.slot * S::STAGE_BYTES);
           const uint32_t fb = bar(S::B_FULL + r.slot);
-          mbar_arrive_expect_tx(fb, kSubTileBytes);
-          const CUtensorMap* m = c < S::NQC ? &tm_k : &tm_v;
-          const int dc = (c < S::NQC ? c : c - S::NQC) * 64;
-          if (p.paged) {
-            tma_load_4d(dst, m, fb, dc, g, 0, c0);
-            tma_load_4d(dst + kSubTileBytes / 2, m, fb, dc, g, 0, c1);
+          const int nsub = part == 0 ? S::NQC : S::NVC;
+          const CUtensorMap* m = part == 0 ? &tm_k : &tm_v;
+          // Rows of the last loaded block at positions >= kv_len hold whatever
+          // the pool holds there; their V rows are zeroed before the stage is
+          // released so that P = 0 times them stays 0 (K rows there are masked
+          // to -inf before the softmax).  This happens at most once per CTA.
+          const int r0 = seg.kv_len - key0;
+          const bool fix = part == 1 && p.paged && r0 > 0 && r0 < kTileN && (r0 % kBlockTokens) != 0;
+          if (!fix) {
+            mbar_arrive_expect_tx(fb, nsub * kSubTileBytes);
+            load_part(m, nsub, dst, fb, c0, c1);
           } else {
-            tma_load_3d(dst, m, fb, dc, g, c0);
-            tma_load_3d(dst + kSubTileBytes / 2, m, fb, dc, g, c1);
+            mbar_arrive_expect_tx(bar(S::B_TMP), nsub * kSubTileBytes);
+            load_part(m, nsub, dst, bar(S::B_TMP), c0, c1);
+            if (!mbar_wait(bar(S::B_TMP), 0, p.status, abort_flag)) {
+              mbar_wait_for(bar(S::B_TMP), 0, kCleanupNs);
+              ok = false;
+              break;
+            }
+            const int r1 = (r0 + kBlockTokens - 1) / kBlockTokens * kBlockTokens;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < nsub; ++c)
+              for (int row = r0; row < r1; ++row) {
+                uint4* rp = reinterpret_cast<uint4*>(sRing + r.slot * S::STAGE_BYTES +
+                                                     c * kSubTileBytes + row * 128);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) rp[u] = z;
+              }
+            fence_proxy_async_smem();
+            mbar_arrive(fb);
           }
           filled |= 1u << r.slot;
           fill_phase = (fill_phase & ~(1u << r.slot)) | (r.phase << r.slot);
-          r.advance(S::NSLOT);
+          r.advance(S::NSTAGE);
         }
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA exits.
-        for (int i = 0; i < S::NSLOT; ++i)
-          if (filled & (1u << i))
-            mbar_wait_for(bar(S::B_FULL + i), (fill_phase >> i) & 1u, 100000000ull);
-        mbar_wait_for(bar(S::B_Q), 0, 100000000ull);
+        for (int i = 0; i < S::NSTAGE; ++i)
+          if (filled & (1u << i)) mbar_wait_for(bar(S::B_FULL + i), (fill_phase >> i) & 1u, kCleanupNs);
+        mbar_wait_for(bar(S::B_Q), 0, kCleanupNs);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
-    Ring r{0, 0u};
-    auto qk = [&](int x, int kslot) {
-      const uint32_t d = tbase + x * kTileN;
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // ---------------------------------------------------- MMA issuer
+      const int x = warp == 1 ? 0 : 1;
+      // Descriptors are built once; sub-tile and k-step offsets are added to
+      // the start-address field (16-byte units; shared addresses stay below
+      // 2^18, so the 14-bit field never carries).
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ + x * S::NQC * kSubTileBytes), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sRing), 16, 1024);             // K-major
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sRing), kSubTileBytes, 1024);  // MN-major
+      constexpr uint32_t kSub16 = kSubTileBytes >> 4;
+      constexpr uint32_t kStage16 = S::STAGE_BYTES >> 4;
+      const uint32_t tS = tbase + x * kTileN;
+      const uint32_t tO = tbase + 2 * kTileN + x * DV;
+      Ring r{0, 0u};
+      bool ok = mbar_wait(bar(S::B_Q), 0, p.status, abort_flag);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int ks = r.slot;
+        const uint32_t kph = r.phase;
+        r.advance(S::NSTAGE);
+        const int vs = r.slot;
+        const uint32_t vph = r.phase;
+        r.advance(S::NSTAGE);
+        // S = Q K^T.  In issue order this follows PV(x, j-1), which read P
+        // from the same TMEM columns.
+        if (!(ok = mbar_wait(bar(S::B_FULL + ks), kph, p.status, abort_flag))) break;
+        const uint64_t kb = dk0 + ks * kStage16;
 #pragma unroll
-      for (int c = 0; c < S::NQC; ++c) {
-        const uint32_t qa = smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes);
-        const uint32_t kb = smem_u32(sRing + ((kslot + c) % S::NSLOT) * kSubTileBytes);
+        for (int c = 0; c < S::NQC; ++c)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(d, sdesc_sw128(qa + 32 * k, 16, 1024), sdesc_sw128(kb + 32 * k, 16, 1024),
-                  S::IDESC_QK, (c | k) ? 1u : 0u);
-      }
-    };
-    auto pv = [&](int x, int vslot, bool acc) {
-      const uint32_t a = tbase + x * kTileN;
-#pragma unroll
-      for (int h = 0; h < S::NVC; ++h) {
-        const uint32_t d = tbase + 2 * kTileN + x * DV + h * 64;
-        const uint32_t vb = smem_u32(sRing + ((vslot + h) % S::NSLOT) * kSubTileBytes);
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + c * kSub16 + 2 * k, S::IDESC_QK,
+                    (c | k) ? 1u : 0u);
+        umma_commit(bar(S::B_S + x));
+        umma_commit(bar(S::B_EMPTY + ks));
+        // O += P V once the softmax group has written P.
+        if (!(ok = mbar_wait(bar(S::B_FULL + vs), vph, p.status, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(S::B_P + x), j & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t vb = dv0 + vs * kStage16;
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k)
-          umma_ts(d, a + 8 * k, sdesc_sw128(vb + 2048 * k, 16384, 1024), S::IDESC_PV,
-                  (acc || k) ? 1u : 0u);
+          umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(bar(S::B_EMPTY + vs));
       }
-    };
-    auto wait_slots = [&](int n) -> bool {
-      for (int c = 0; c < n; ++c) {
-        if (!warp_wait(bar(S::B_FULL + r.slot), r.phase, p.status, abort_flag)) return false;
-        r.advance(S::NSLOT);
-      }
-      return true;
-    };
-    bool ok = warp_wait(bar(S::B_Q), 0, p.status, abort_flag);
-    if (ok) {
-      const int kslot = r.slot;
-      ok = wait_slots(S::NQC);
       if (ok) {
-        tc_fence_after();
-        if (lane == 0) {
-          qk(0, kslot);
-          umma_commit(bar(S::B_S + 0));
-          qk(1, kslot);
-          umma_commit(bar(S::B_S + 1));
-          for (int c = 0; c < S::NQC; ++c) umma_commit(bar(S::B_EMPTY + (kslot + c) % S::NSLOT));
-        }
-        __syncwarp();
+        umma_commit(bar(S::B_O + x));
+      } else {
+        // Every MMA issued so far must finish before TMEM is freed.
+        umma_commit(bar(S::B_FINAL + x));
+        mbar_wait_for(bar(S::B_FINAL + x), 0, kCleanupNs);
       }
     }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int vslot = r.slot;
-      if (!(ok = wait_slots(S::NVC))) break;
-      if (p.paged && j == n_kv - 1) {
-        // Rows of the last loaded block at positions >= kv_len hold whatever
-        // the pool holds there; zero their V rows so that P = 0 times them
-        // stays 0 (K rows there are masked to -inf before the softmax).
-        const int key0 = k_lo + j * kTileN;
-        const int r0 = seg.kv_len - key0;
-        if (r0 > 0 && r0 < kTileN && (r0 % kBlockTokens) != 0) {
-          const int r1 = (r0 + kBlockTokens - 1) / kBlockTokens * kBlockTokens;
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          for (int h = 0; h < S::NVC; ++h) {
-            uint8_t* base = sRing + ((vslot + h) % S::NSLOT) * kSubTileBytes;
-            for (int idx = lane; idx < (r1 - r0) * 8; idx += 32)
-              *reinterpret_cast<uint4*>(base + (r0 + idx / 8) * 128 + (idx % 8) * 16) = z;
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-      }
-      if (!(ok = warp_wait(bar(S::B_P + 0), j & 1, p.status, abort_flag))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        pv(0, vslot, j > 0);
-        if (j == n_kv - 1) umma_commit(bar(S::B_O + 0));
-      }
-      __syncwarp();
-      int nk = -1;
-      if (j + 1 < n_kv) {
-        nk = r.slot;
-        if (!(ok = wait_slots(S::NQC))) break;
-        tc_fence_after();
-        if (lane == 0) {
-          qk(0, nk);
-          umma_commit(bar(S::B_S + 0));
-        }
-        __syncwarp();
-      }
-      if (!(ok = warp_wait(bar(S::B_P + 1), j & 1, p.status, abort_flag))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        pv(1, vslot, j > 0);
-        for (int h = 0; h < S::NVC; ++h) umma_commit(bar(S::B_EMPTY + (vslot + h) % S::NSLOT));
-        if (j == n_kv - 1) umma_commit(bar(S::B_O + 1));
-        if (nk >= 0) {
-          qk(1, nk);
-          umma_commit(bar(S::B_S + 1));
-          for (int c = 0; c < S::NQC; ++c) umma_commit(bar(S::B_EMPTY + (nk + c) % S::NSLOT));
-        }
-      }
-      __syncwarp();
-    }
-    if (!ok && lane == 0) {
-      // Every MMA issued so far must finish before TMEM is freed.
-      umma_commit(bar(S::B_FINAL));
-      mbar_wait_for(bar(S::B_FINAL), 0, 100000000ull);
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<kRegsHigh>();
     // ------------------------------------------------------ softmax + epilogue
     const int x = (warp - 4) >> 2;
     const int wq = warp & 3;
@@ -346,9 +336,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (key0 + c > lim) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      // Row max: eight independent chains, then a tree.
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * sl);
       if (j == 0) {
         m = m_new;
@@ -374,22 +369,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_st_wait();
         }
       }
+      // p = 2^(s * scale * log2(e) - m), two lanes of work per packed FMA;
+      // P is stored to TMEM in two halves so the first store overlaps the
+      // second half's exponentials.
       const float mb = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
-      uint32_t pk[2][32];
+      const float2 sl2 = make_float2(sl, sl);
+      const float2 nmb2 = make_float2(-mb, -mb);
+      float rs8[8];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float a = ex2_approx(fmaf(sv[2 * c], sl, -mb));
-        const float b = ex2_approx(fmaf(sv[2 * c + 1], sl, -mb));
-        rs += a + b;
-        pk[c >> 5][c & 31] = pack_bf16x2(a, b);
+      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+      uint32_t pk0[32], pk1[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
+        const float a = ex2_approx(xx.x);
+        const float b = ex2_approx(xx.y);
+        rs8[c & 7] += a + b;
+        pk0[c] = pack_bf16x2(a, b);
       }
-      tmem_st32(tS, pk[0]);
-      tmem_st32(tS + 32, pk[1]);
+      tmem_st32(tS, pk0);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 xx = ffma2(make_float2(sv[64 + 2 * c], sv[64 + 2 * c + 1]), sl2, nmb2);
+        const float a = ex2_approx(xx.x);
+        const float b = ex2_approx(xx.y);
+        rs8[c & 7] += a + b;
+        pk1[c] = pack_bf16x2(a, b);
+      }
+      tmem_st32(tS + 32, pk1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(S::B_P + x));
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
     }
     if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);
     if (ok) {
@@ -449,7 +460,7 @@ template <int DQ, int DV>
 cudaError_t launch_chunk_attn_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const AttnParams& p, int grid,
                                 cudaStream_t stream) {
-  constexpr int smem = attn_smem_bytes(DQ);
+  constexpr int smem = attn_smem_bytes(DQ, DV);
   static_assert(smem <= kSmemLimit, "shared memory budget");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
