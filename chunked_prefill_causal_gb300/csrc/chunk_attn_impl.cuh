@@ -19,10 +19,14 @@
 //               = one K tile or one V tile, one full/empty mbarrier pair).
 //   warp 1, 3   MMA issuers, one elected lane each: warp 1 for query tile A,
 //               warp 3 for tile B.  S = Q K^T into TMEM (kind::f16, bf16 in,
-//               f32 accumulate), then O += P V with P read from TMEM.  Two
-//               issuers let one tile's MMAs run while the other waits for its
-//               softmax: a wait, commit or fence between MMA batches in the
-//               issuing thread leaves the tensor core idle otherwise.
+//               f32 accumulate), then O += P V with P read from TMEM.  Each
+//               issuer emits blocks [PV(x, j-1), QK(x, j)] and the two take
+//               turns (a shared counter), so the tensor core runs A's block j,
+//               B's block j, A's block j+1, ...: the softmax of one tile runs
+//               while the tensor core works on the other tile's block, and the
+//               waits, commits and fences of one issuer (each leaves the tensor
+//               core idle if it sits between the MMAs of a single issuing
+//               thread) overlap the other issuer's MMAs.
 //   warp 2      allocates and frees the 512 TMEM columns.
 //   warps 4-7   softmax + epilogue of query tile A; warps 8-11 of tile B.
 //               Each thread owns one query row = one TMEM lane, so row max and
@@ -103,6 +107,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSTAGE * S::STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
+  volatile int* turn = reinterpret_cast<volatile int*>(tmem_slot + 2);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -128,6 +133,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
+    *turn = 0;
     mbar_init(bar(S::B_Q), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(S::B_S + x), 1);
@@ -266,39 +272,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t tS = tbase + x * kTileN;
       const uint32_t tO = tbase + 2 * kTileN + x * DV;
       Ring r{0, 0u};
+      int pvs = 0;          // stage of V(j-1)
+      uint32_t pvph = 0u;
       bool ok = mbar_wait(bar(S::B_Q), 0, p.status, abort_flag);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int ks = r.slot;
-        const uint32_t kph = r.phase;
-        r.advance(S::NSTAGE);
-        const int vs = r.slot;
-        const uint32_t vph = r.phase;
-        r.advance(S::NSTAGE);
-        // S = Q K^T.  In issue order this follows PV(x, j-1), which read P
-        // from the same TMEM columns.
-        if (!(ok = mbar_wait(bar(S::B_FULL + ks), kph, p.status, abort_flag))) break;
-        const uint64_t kb = dk0 + ks * kStage16;
+      // Block j = [PV(x, j-1) if j > 0][QK(x, j) if j < n_kv]; blocks run in
+      // the global order A0 B0 A1 B1 ...: block j of issuer x is number 2j+x.
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        int ks = 0, vs = 0;
+        uint32_t kph = 0u, vph = 0u;
+        if (j < n_kv) {
+          ks = r.slot;
+          kph = r.phase;
+          r.advance(S::NSTAGE);
+          vs = r.slot;
+          vph = r.phase;
+          r.advance(S::NSTAGE);
+        }
+        if (j > 0) {
+          if (!(ok = mbar_wait(bar(S::B_FULL + pvs), pvph, p.status, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(S::B_P + x), (j - 1) & 1, p.status, abort_flag))) break;
+          tc_fence_after();
+        }
+        if (j < n_kv && !(ok = mbar_wait(bar(S::B_FULL + ks), kph, p.status, abort_flag))) break;
+        // Take the turn (bounded spin; gives up if another role aborted).
+        if (*turn != 2 * j + x) {
+          const uint64_t t0 = globaltimer_ns();
+          while (*turn != 2 * j + x) {
+            if (*abort_flag) { ok = false; break; }
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+              record_status(p.status, kStatusTimeout);
+              *abort_flag = 1u;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+        }
+        if (j > 0) {
+          // O += P V for tile j-1 (P read from TMEM, V from the ring).
+          const uint64_t vb = dv0 + pvs * kStage16;
 #pragma unroll
-        for (int c = 0; c < S::NQC; ++c)
+          for (int k = 0; k < kTileN / 16; ++k)
+            umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 1 || k > 0) ? 1u : 0u);
+        }
+        if (j < n_kv) {
+          // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
+          // same TMEM columns, in issue order.
+          const uint64_t kb = dk0 + ks * kStage16;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + c * kSub16 + 2 * k, S::IDESC_QK,
-                    (c | k) ? 1u : 0u);
-        umma_commit(bar(S::B_S + x));
-        umma_commit(bar(S::B_EMPTY + ks));
-        // O += P V once the softmax group has written P.
-        if (!(ok = mbar_wait(bar(S::B_FULL + vs), vph, p.status, abort_flag))) break;
-        if (!(ok = mbar_wait(bar(S::B_P + x), j & 1, p.status, abort_flag))) break;
-        tc_fence_after();
-        const uint64_t vb = dv0 + vs * kStage16;
+          for (int c = 0; c < S::NQC; ++c)
 #pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)
-          umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(bar(S::B_EMPTY + vs));
+            for (int k = 0; k < 4; ++k)
+              umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + c * kSub16 + 2 * k, S::IDESC_QK,
+                      (c | k) ? 1u : 0u);
+        }
+        *turn = 2 * j + x + 1;
+        if (j < n_kv) {
+          umma_commit(bar(S::B_S + x));
+          umma_commit(bar(S::B_EMPTY + ks));
+        }
+        if (j > 0) umma_commit(bar(S::B_EMPTY + pvs));
+        if (j == n_kv) umma_commit(bar(S::B_O + x));
+        pvs = vs;
+        pvph = vph;
       }
-      if (ok) {
-        umma_commit(bar(S::B_O + x));
-      } else {
+      if (!ok) {
+        *abort_flag = 1u;  // the partner issuer may be waiting for this turn
         // Every MMA issued so far must finish before TMEM is freed.
         umma_commit(bar(S::B_FINAL + x));
         mbar_wait_for(bar(S::B_FINAL + x), 0, kCleanupNs);
@@ -336,14 +375,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (key0 + c > lim) sv[c] = -INFINITY;
       }
-      // Row max: eight independent chains, then a tree.
+      // Row max: eight independent chains of 3-input max, then a tree.
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 8; c < 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m, mx * sl);
       if (j == 0) {
         m = m_new;
@@ -375,16 +416,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float mb = (m == -INFINITY) ? 0.f : m;
       const float2 sl2 = make_float2(sl, sl);
       const float2 nmb2 = make_float2(-mb, -mb);
-      float rs8[8];
+      float2 rs4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+      for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
       uint32_t pk0[32], pk1[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
         const float a = ex2_approx(xx.x);
         const float b = ex2_approx(xx.y);
-        rs8[c & 7] += a + b;
+        rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
         pk0[c] = pack_bf16x2(a, b);
       }
       tmem_st32(tS, pk0);
@@ -393,14 +434,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float2 xx = ffma2(make_float2(sv[64 + 2 * c], sv[64 + 2 * c + 1]), sl2, nmb2);
         const float a = ex2_approx(xx.x);
         const float b = ex2_approx(xx.y);
-        rs8[c & 7] += a + b;
+        rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
         pk1[c] = pack_bf16x2(a, b);
       }
       tmem_st32(tS + 32, pk1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(S::B_P + x));
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 rs2 = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
+      l += rs2.x + rs2.y;
     }
     if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);
     if (ok) {
