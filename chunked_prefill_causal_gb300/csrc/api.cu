@@ -280,6 +280,20 @@ int build_varlen_plan(const int32_t* cu, const int32_t* ctx, int32_t batch, Varl
 
 }  // namespace
 
+namespace vpp {
+// Entry into the chunk-attention planner and launcher for other translation
+// units of this library (same contract as vpp_chunk_attn_ex).
+int run_chunk_attn(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                   const int32_t* block_table, int32_t num_blocks, int64_t prefix_len,
+                   int64_t chunk_len, int heads, int kv_heads, int head_dim_qk, int head_dim_v,
+                   float softmax_scale, int num_splits, void* out, float* lse, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  return chunk_attn_impl(q, q_dtype, k_cache, v_cache, block_table, num_blocks, prefix_len,
+                         chunk_len, heads, kv_heads, head_dim_qk, head_dim_v, softmax_scale,
+                         num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+}  // namespace vpp
+
 extern "C" {
 
 const char* vpp_status_string(int status) {

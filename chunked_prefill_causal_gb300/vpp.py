@@ -33,6 +33,8 @@ SIGNATURES = {
     "vpp_chunk_attn_ex": ([_c_void_p, _int, _c_void_p, _c_void_p, _c_void_p, _i32, _i64, _i64, _int,
                            _int, _int, _int, _f32, _int, _c_void_p, _c_void_p, _c_void_p, _sz,
                            _c_void_p], _int),
+    "vpp_chunk_attn_noalloc": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64, _i64, _int, _int,
+                                _int, _int, _f32, _int, _c_void_p, _c_void_p, _c_void_p], _int),
     "vpp_chunk_attn_workspace_size": ([_int, _i64, _i64, _int, _int, _int, _int, _int], _sz),
     "vpp_chunk_attn_num_splits": ([_i64, _i64, _int, _int, _int, _int, _int], _int),
     "vpp_mixed_attn": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
@@ -188,6 +190,25 @@ def vpp_chunk_attn_ex(q, k_cache, v_cache, prefix_len, block_table=None, out=Non
         _ptr(q), qd, _ptr(k_cache), _ptr(v_cache), _ptr(block_table), nb, int(prefix_len), C, H, Hkv,
         dq, dv, float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace), wbytes,
         _stream(stream)))
+    return out
+
+
+def vpp_chunk_attn_noalloc(q, k_cache, v_cache, prefix_len, block_table=None, out=None, lse=None,
+                           softmax_scale=0.0, num_splits=0, stream=None):
+    """Chunk attention whose key-split partials use the library's fixed 32 MiB
+    device array instead of a workspace (for callers that cannot allocate);
+    bf16 q only.  Calls on one device must not overlap on the GPU."""
+    _need_cuda(q, k_cache, v_cache, block_table, out, lse)
+    C, H, dq = q.shape
+    Hkv = k_cache.shape[-2]
+    dv = v_cache.shape[-1]
+    if q.dtype != torch.bfloat16:
+        raise ValueError("vpp_chunk_attn_noalloc takes bf16 q")
+    if out is None:
+        out = torch.empty((C, H, dv), dtype=torch.bfloat16, device=q.device)
+    _check("vpp_chunk_attn_noalloc", load().vpp_chunk_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), k_cache.shape[0], int(prefix_len), C, H,
+        Hkv, dq, dv, float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse), _stream(stream)))
     return out
 
 

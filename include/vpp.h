@@ -143,6 +143,34 @@ int vpp_chunk_attn_ex(const void *q, int q_dtype, const void *k_cache,
                       int num_splits, void *out, float *lse, void *workspace,
                       size_t workspace_bytes, void *stream);
 
+/*
+ * Chunk attention without any allocation and without a caller workspace.
+ * The pages have no counterpart to this entry point; it serves callers that
+ * may not allocate device memory on their execution path and cannot hand
+ * over scratch space (for example a plug-in whose host runtime owns all
+ * device memory, or a binding that exposes only the plain signature).
+ *
+ * Same arguments and results as vpp_chunk_attn_ex with q_dtype = VPP_BF16 and
+ * no workspace.  When the key range is split, the float32 partials live in a
+ * fixed 32 MiB array in device memory that the library holds on every GPU
+ * that loads it, until the process exits.  Calls whose partials would exceed
+ * 32 MiB (num_splits x chunk_len x heads x (head_dim_v + 1) x 4 bytes, see
+ * vpp_chunk_attn_workspace_size) return VPP_ERR_WORKSPACE and launch nothing.
+ * The first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture.  All calls
+ * on a device share the array and it keeps the last call's contents (nothing
+ * in it needs to start at zero), so calls that overlap on the GPU race: issue
+ * them on one stream or synchronise between them.  Calls no allocating
+ * routine.
+ */
+int vpp_chunk_attn_noalloc(const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *block_table,
+                           int32_t num_blocks, int64_t prefix_len,
+                           int64_t chunk_len, int heads, int kv_heads,
+                           int head_dim_qk, int head_dim_v,
+                           float softmax_scale, int num_splits, void *out,
+                           float *lse, void *stream);
+
 /* Workspace bytes vpp_chunk_attn_ex needs for these arguments (0 if none). */
 size_t vpp_chunk_attn_workspace_size(int q_dtype, int64_t prefix_len,
                                      int64_t chunk_len, int heads,
