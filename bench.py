@@ -37,6 +37,29 @@ import torch  # noqa: E402
 from chunked_prefill_causal_gb300 import workloads as W  # noqa: E402
 
 METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens/s"
+
+# DRAM bytes (read + write) per launch of the chunk-attention kernel, averaged
+# over the 8 launches of one long128k step, from one ncu capture
+# (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
+# digest is recorded with it; any change to them makes the figure stale (null).
+TRAFFIC = {"long128k": {"sources_sha256": "7c36a21a363d67e387c1560676e33157d7e5f4a5895506d79c3fd4fb61441c62", "bytes_per_launch": 1.2117e9}}
+KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
+
+
+def kernel_sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "chunked_prefill_causal_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    rec = TRAFFIC.get(workload)
+    if rec and rec["sources_sha256"] == kernel_sources_digest():
+        return rec["bytes_per_launch"]
+    return None
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -329,6 +352,13 @@ def run_ours(args, dist_):
     late = [c for c in per_chunk if c["k"] >= len(chunks) // 2]
     late_tf = sum(flops[c["k"]] for c in late) / (sum(c["ms"] for c in late) / 1e3) / 1e12
 
+    # Algorithmic DRAM bytes of one chunk-attention launch, averaged over the
+    # step: Q and out once, lse, and every visible K/V row once.
+    alg_bytes = statistics.mean(
+        C * w.heads * (w.head_dim_qk + w.head_dim_v) * 2 + C * w.heads * 4
+        + (P + C) * w.kv_heads * (w.head_dim_qk + w.head_dim_v) * 2 for P, C in chunks)
+    traffic = args.traffic if args.traffic is not None else recorded_traffic(w.name)
+
     # KV append bandwidth on this workload's chunks (bytes read + written).
     app_bytes = [2 * C * w.kv_heads * (w.head_dim_qk + w.head_dim_v) * 2 for _, C in chunks]
 
@@ -390,7 +420,10 @@ def run_ours(args, dist_):
             "clocks": clk, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                         "traffic": args.traffic, "peak_source": f"bf16_tflops_sustained ({pk_src})",
+                         "traffic": traffic,
+                         "algorithmic_bytes": round(alg_bytes),
+                         "traffic_vs_algorithmic": round(traffic / alg_bytes, 3) if traffic else None,
+                         "peak_source": f"bf16_tflops_sustained ({pk_src})",
                          "frac_of_burst": round(achieved / peak_tf_burst, 4)},
             "cpu_baseline": cpu,
             "per_chunk": per_chunk,

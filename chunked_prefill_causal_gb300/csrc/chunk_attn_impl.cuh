@@ -118,10 +118,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   while (si + 1 < p.n_segs && p.segs[si + 1].cta_begin <= static_cast<int>(blockIdx.x)) ++si;
   const AttnSeg& seg = p.segs[si];
   const int local = static_cast<int>(blockIdx.x) - seg.cta_begin;
+  // CTA order: key range fastest, then query-tile pairs (heaviest first), then
+  // kv head, so the CTAs resident at one time read the same kv head's K/V
+  // tiles and share them through L2.
   const int split = local % seg.n_splits;
   const int rest = local / seg.n_splits;
-  const int g = rest % p.kv_heads;
-  const int pair = seg.n_pairs - 1 - rest / p.kv_heads;  // heaviest pairs first
+  const int pair = seg.n_pairs - 1 - rest % seg.n_pairs;
+  const int g = rest / seg.n_pairs;
   const int G = p.group;
   const int T = kTileM / G;       // tokens per query tile
   const int tok0 = pair * 2 * T;  // first token of tile A (segment-relative)
