@@ -190,25 +190,34 @@ def mixed_block_tables(m: MixedWorkload, slack_blocks: int = 7):
     return table, pool
 
 
-def sample_rows(n_tokens_per_chunk, heads: int, n_rows: int, seed: int, tile_tokens: int = 16):
+def sample_rows(n_tokens_per_chunk, heads, n_rows: int, seed: int, tile_tokens: int = 16):
     """Seeded, stratified sample of (chunk, token, head) rows.
 
+    ``heads`` is a head count or an explicit list of heads to draw from.
     Equal rows per chunk; each chunk always includes its first and last
     token and tokens on both sides of tile boundaries (multiples of
     ``tile_tokens``) so that diagonal-tile edges are exercised.
     """
     rng = np.random.default_rng(seed)
+    head_pool = np.arange(heads) if np.isscalar(heads) else np.asarray(heads)
     n_chunks = len(n_tokens_per_chunk)
     per = max(1, n_rows // n_chunks)
     rows = []
     for ci, C in enumerate(n_tokens_per_chunk):
         fixed = {0, C - 1}
-        for b in rng.choice(max(1, C // tile_tokens), size=min(8, max(1, C // tile_tokens)), replace=False):
+        n_b = max(1, C // tile_tokens)
+        for b in rng.choice(n_b, size=min(8, n_b), replace=False):
             t = int(b) * tile_tokens
             fixed.update({max(0, t - 1), min(C - 1, t)})
-        toks = list(fixed)
+        toks = sorted(fixed)
         toks += list(rng.integers(0, C, size=max(0, per - len(toks))))
         toks = np.array(toks[:per])
-        hs = rng.integers(0, heads, size=len(toks))
+        hs = rng.choice(head_pool, size=len(toks))
         rows += [(ci, int(t), int(h)) for t, h in zip(toks, hs)]
     return rows
+
+
+def head_subset(heads: int, n: int, seed: int):
+    """A seeded subset of n query heads (sorted)."""
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(heads, size=min(n, heads), replace=False))
