@@ -11,6 +11,7 @@
 
 #include "chunk_attn.cuh"
 #include "common.cuh"
+#include "decode.cuh"
 #include "vpp.h"
 
 namespace vpp {
@@ -264,6 +265,26 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   return VPP_OK;
 }
 
+// Rows of a mixed batch served by the decode kernel, and the workspace their
+// multi-range partials need.
+bool is_decode_row(const int32_t* cu, int b, int heads, int kv_heads, int dq, int dv) {
+  return cu[b + 1] - cu[b] == 1 && decode_supported(dq, dv, heads, kv_heads);
+}
+
+size_t decode_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int heads,
+                       int kv_heads, int dq, int dv) {
+  int64_t items = 0;
+  bool any_multi = false;
+  for (int b = 0; b < batch; ++b) {
+    if (!is_decode_row(cu, b, heads, kv_heads, dq, dv)) continue;
+    const int64_t n = ceil_div(std::max<int32_t>(ctx[b], 1), kDecodeSplitTokens);
+    items += n;
+    any_multi |= n > 1;
+  }
+  if (!any_multi) return 0;
+  return round_up((size_t)items * heads * dv * 4, 256) + round_up((size_t)items * heads * 4, 256);
+}
+
 int build_varlen_plan(const int32_t* cu, const int32_t* ctx, int32_t batch, VarlenPlan* plan) {
   if (!cu || !ctx || batch <= 0 || batch > kMaxBatch) return VPP_ERR_INVALID;
   if (cu[0] != 0) return VPP_ERR_INVALID;
@@ -411,8 +432,6 @@ int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,
                    int heads, int kv_heads, int head_dim_qk, int head_dim_v,
                    float softmax_scale, void* out, float* lse, void* workspace,
                    size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (!q || !k_cache || !v_cache || !block_table || !out) return VPP_ERR_INVALID;
   if (num_blocks <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
   if (int r = check_heads(heads, kv_heads)) return r;
@@ -451,12 +470,21 @@ int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,
   p.lse_stride = total_q;
   p.status = ds->status;
 
+  // Decode rows go to the split-KV decode kernel when it supports the shape;
+  // every other sequence with queries becomes one chunk-attention segment.
+  const size_t dws = decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
+                                     head_dim_v);
+  if (dws > 0 && (!workspace || workspace_bytes < dws || !aligned16(workspace)))
+    return VPP_ERR_WORKSPACE;
+
   // Every sequence with queries becomes one segment; segments are ordered by
   // per-CTA work (keys per CTA) so the heaviest CTAs start first.
   int order[kMaxBatch];
   int n = 0;
   for (int b = 0; b < batch; ++b)
-    if (cu_seqlens_q[b + 1] > cu_seqlens_q[b]) order[n++] = b;
+    if (cu_seqlens_q[b + 1] > cu_seqlens_q[b] &&
+        !is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v))
+      order[n++] = b;
   std::stable_sort(order, order + n, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
   for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
     const int cnt = std::min(kMaxAttnSegs, n - i0);
@@ -481,20 +509,59 @@ int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,
         cudaSuccess)
       return VPP_ERR_CUDA;
   }
+
+  // Decode rows, longest context first.
+  static DecodeParams zero_dp;
+  DecodeParams dp = zero_dp;
+  int drows[kMaxBatch];
+  int nd = 0;
+  for (int b = 0; b < batch; ++b)
+    if (is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v) && ctx_lens[b] > 0)
+      drows[nd++] = b;
+  if (nd > 0) {
+    std::stable_sort(drows, drows + nd, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
+    int64_t items = 0;
+    for (int i = 0; i < nd; ++i) {
+      const int b = drows[i];
+      dp.rows[i].b = b;
+      dp.rows[i].q_row = cu_seqlens_q[b];
+      dp.rows[i].ctx = ctx_lens[b];
+      dp.rows[i].item0 = (int32_t)items;
+      items += ceil_div(ctx_lens[b], kDecodeSplitTokens);
+    }
+    if (items > INT32_MAX) return VPP_ERR_INVALID;
+    dp.n_rows = nd;
+    dp.heads = heads;
+    dp.kv_heads = kv_heads;
+    dp.split_tokens = kDecodeSplitTokens;
+    dp.num_blocks = num_blocks;
+    dp.max_blocks_per_seq = max_blocks_per_seq;
+    dp.scale_log2 = p.scale_log2;
+    dp.q = static_cast<const uint16_t*>(q);
+    dp.k_cache = static_cast<const uint16_t*>(k_cache);
+    dp.v_cache = static_cast<const uint16_t*>(v_cache);
+    dp.block_table = block_table;
+    dp.out = static_cast<uint16_t*>(out);
+    dp.lse = lse;
+    dp.lse_stride = total_q;
+    if (dws > 0) {
+      dp.ws_o = static_cast<float*>(workspace);
+      dp.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           round_up((size_t)items * heads * head_dim_v * 4, 256));
+    }
+    dp.status = ds->status;
+    if (launch_decode(dp, (int)items, head_dim_qk, ds->num_sms, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+  }
   return VPP_OK;
 }
 
 size_t vpp_mixed_attn_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
                                      int32_t batch, int heads, int kv_heads, int head_dim_qk,
                                      int head_dim_v) {
-  (void)cu_seqlens_q;
-  (void)ctx_lens;
-  (void)batch;
-  (void)heads;
-  (void)kv_heads;
-  (void)head_dim_qk;
-  (void)head_dim_v;
-  return 0;
+  if (!cu_seqlens_q || !ctx_lens || batch <= 0 || batch > kMaxBatch) return 0;
+  if (check_heads(heads, kv_heads) != VPP_OK) return 0;
+  return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v);
 }
 
 int vpp_last_device_status(void* stream, int* code) {

@@ -1,0 +1,375 @@
+// decode.cu -- a8: split-KV attention of single-token decode rows over a paged
+// KV cache (the decode half of a mixed micro-batch).
+//
+// "VPP: Virtual Pipeline Parallelism for Efficient Chunked Prefill in
+// Long-Context LLM Inference" (technical review), §2.1: decode produces one
+// token per step and must read the whole accumulated KV cache, so it is
+// bound by memory bandwidth.  "Revisiting Pipeline Parallelism for LLM
+// Serving", section "预备知识": a decode request contributes one token to a
+// mixed micro-batch.  The arithmetic is Eq. (1) of the VPP review (§2.2) for
+// a query at position ctx-1 that sees keys 0..ctx-1.
+//
+// Work item = (row, key range of split_tokens keys).  One CTA per item:
+//   warp Hkv (last)   producer: for every 16-token step, one 1-D bulk copy of
+//                     the step's K rows and one of its V rows (16 tokens x all
+//                     kv heads are contiguous inside a 64-token block), into a
+//                     ring of shared-memory stages with full/empty mbarriers.
+//   warps 0..Hkv-1    warp h serves kv head h and its G query heads.  Scores:
+//                     8 lanes per token (D/8 dims each, 4 tokens per pass),
+//                     summed with three xor-shuffles.  Online softmax per head
+//                     (running max and denominator, rescale only when the max
+//                     grows by more than 2^8).  P V: each lane owns D/32
+//                     output dims of every head; p is passed through shared
+//                     memory.
+// A range's result is final when the row has one range; otherwise the float32
+// partial output and its LSE go to the workspace and decode_merge combines
+// them ("02 · 并行策略与 PP 切分" note, §7).  HBM-bound: the algorithmic bytes
+// are ctx x Hkv x (dq + dv) x 2 per row plus q, out and the partials.
+#include <algorithm>
+
+#include "common.cuh"
+#include "decode.cuh"
+#include "ptx.cuh"
+
+namespace vpp {
+namespace {
+
+constexpr int kStepTokens = 16;
+constexpr int kDecodeSmem = 196608 + 4096 + 256;  // ring + p exchange + barriers
+constexpr float kLn2d = 0.69314718055994530942f;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int DPL = D / 8;     // score dims per lane (8 lanes per token)
+  constexpr int OPL = D / 32;    // output dims per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int hkv = p.kv_heads;
+  const int row_bytes = hkv * D * 2;                 // one token, all kv heads
+  const int stage_bytes = 2 * kStepTokens * row_bytes;  // K then V
+  const int nstage = min(8, 196608 / stage_bytes);
+  float* pbuf = reinterpret_cast<float*>(smem + 196608);  // [hkv][16][G]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 196608 + 8 * kStepTokens * 8 * 4);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 16);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------- work item
+  int lo = 0, hi = p.n_rows - 1;
+  const int item = blockIdx.x;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.rows[mid].item0 <= item) lo = mid; else hi = mid - 1;
+  }
+  const DecodeRow row = p.rows[lo];
+  const int split = item - row.item0;
+  const int n_splits = (row.ctx + p.split_tokens - 1) / p.split_tokens;
+  const int t_begin = split * p.split_tokens;
+  const int t_end = min(row.ctx, t_begin + p.split_tokens);
+  const int n_steps = (t_end - t_begin + kStepTokens - 1) / kStepTokens;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int i = 0; i < nstage; ++i) {
+      mbar_init(smem_u32(&bars[i]), 1);
+      mbar_init(smem_u32(&bars[8 + i]), hkv);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == hkv) {
+    // ------------------------------------------------------ producer
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0u;
+      uint32_t filled = 0u, fill_phase = 0u;
+      bool ok = true;
+      for (int s = 0; s < n_steps; ++s) {
+        const int t0 = t_begin + s * kStepTokens;
+        const int nt = min(kStepTokens, t_end - t0);
+        int blk = p.block_table[static_cast<int64_t>(row.b) * p.max_blocks_per_seq + t0 / kBlockTokens];
+        if (blk < 0 || blk >= p.num_blocks) {
+          record_status(p.status, kStatusInvalid);
+          blk = -1;
+        }
+        if (!mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&bars[slot]);
+        const uint32_t dst = smem_u32(smem + slot * stage_bytes);
+        if (blk >= 0) {
+          const int64_t off = (static_cast<int64_t>(blk) * kBlockTokens + t0 % kBlockTokens) * hkv * D;
+          const uint32_t bytes = static_cast<uint32_t>(nt * row_bytes);
+          mbar_arrive_expect_tx(full, 2 * bytes);
+          bulk_g2s(dst, p.k_cache + off, bytes, full);
+          bulk_g2s(dst + kStepTokens * row_bytes, p.v_cache + off, bytes, full);
+        } else {
+          mbar_arrive(full);  // invalid block: the step's rows are skipped
+        }
+        filled |= 1u << slot;
+        fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
+        if (++slot == nstage) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        for (int i = 0; i < nstage; ++i)
+          if (filled & (1u << i)) mbar_wait_for(smem_u32(&bars[i]), (fill_phase >> i) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp < hkv) {
+    // ------------------------------------------------------ kv head `warp`
+    const int h = warp;
+    const int tt = lane >> 3;  // token within a pass of 4
+    const int r = lane & 7;    // dim group
+    const uint16_t* qrow = p.q + static_cast<int64_t>(row.q_row) * p.heads * D;
+    float qf[G][DPL];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + (h * G + j) * D + r * DPL);
+#pragma unroll
+      for (int c = 0; c < DPL / 8; ++c) {
+        const uint4 w = __ldg(src + c);
+        bf16x2_to_f32(w.x, qf[j][8 * c + 0], qf[j][8 * c + 1]);
+        bf16x2_to_f32(w.y, qf[j][8 * c + 2], qf[j][8 * c + 3]);
+        bf16x2_to_f32(w.z, qf[j][8 * c + 4], qf[j][8 * c + 5]);
+        bf16x2_to_f32(w.w, qf[j][8 * c + 6], qf[j][8 * c + 7]);
+      }
+    }
+    const float sl = p.scale_log2;
+    float m[G], lpart[G], o[G][OPL];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      m[j] = -INFINITY;
+      lpart[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < OPL; ++i) o[j][i] = 0.f;
+    }
+    float* pw = pbuf + h * kStepTokens * G;
+    int slot = 0;
+    uint32_t phase = 0u;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      const int t0 = t_begin + s * kStepTokens;
+      const int nt = min(kStepTokens, t_end - t0);
+      ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint8_t* kst = smem + slot * stage_bytes;
+      const uint8_t* vst = kst + kStepTokens * row_bytes;
+      // Scores of this step's 16 tokens (4 passes of 4 tokens).
+      float sc[4][G];
+#pragma unroll
+      for (int ps = 0; ps < 4; ++ps) {
+        const int t = 4 * ps + tt;
+        float acc[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) acc[j] = 0.f;
+        if (t < nt) {
+          const uint4* kr = reinterpret_cast<const uint4*>(kst + t * row_bytes + h * D * 2 + r * DPL * 2);
+#pragma unroll
+          for (int c = 0; c < DPL / 8; ++c) {
+            const uint4 w = kr[c];
+            float kf[8];
+            bf16x2_to_f32(w.x, kf[0], kf[1]);
+            bf16x2_to_f32(w.y, kf[2], kf[3]);
+            bf16x2_to_f32(w.z, kf[4], kf[5]);
+            bf16x2_to_f32(w.w, kf[6], kf[7]);
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[j] = fmaf(qf[j][8 * c + e], kf[e], acc[j]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float v = acc[j];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          sc[ps][j] = (t < nt) ? v * sl : -INFINITY;
+        }
+      }
+      // Online softmax, per query head.
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float mx = fmax3(fmaxf(sc[0][j], sc[1][j]), sc[2][j], sc[3][j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m[j] + 8.0f || m[j] == -INFINITY) {  // warp-uniform
+          const float f = (m[j] == -INFINITY) ? 0.f : ex2_approx(m[j] - mx);
+          lpart[j] *= f;
+#pragma unroll
+          for (int i = 0; i < OPL; ++i) o[j][i] *= f;
+          m[j] = mx;
+        }
+        float ps_sum = 0.f;
+#pragma unroll
+        for (int ps = 0; ps < 4; ++ps) {
+          const float pv = ex2_approx(sc[ps][j] - m[j]);
+          ps_sum += pv;
+          if (r == 0) pw[(4 * ps + tt) * G + j] = pv;
+        }
+        if (r == 0) lpart[j] += ps_sum;
+      }
+      __syncwarp();
+      // O += P V over the step's tokens.
+      for (int t = 0; t < nt; ++t) {
+        float pv[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) pv[j] = pw[t * G + j];
+        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vst + t * row_bytes + h * D * 2) + lane * OPL;
+        float vf[OPL];
+        if (OPL == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(vr);
+          bf16x2_to_f32(w.x, vf[0], vf[1 % OPL]);
+          bf16x2_to_f32(w.y, vf[2 % OPL], vf[3 % OPL]);
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(vr);
+          bf16x2_to_f32(w, vf[0], vf[1 % OPL]);
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+          for (int i = 0; i < OPL; ++i) o[j][i] = fmaf(pv[j], vf[i], o[j][i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
+      if (++slot == nstage) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float l = lpart[j];
+#pragma unroll
+        for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
+        const float inv = 1.f / l;
+        const float lse_v = m[j] * kLn2d + logf(l);
+        const int hq = h * G + j;
+        if (n_splits == 1) {
+          uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + lane * OPL;
+          if (OPL == 4) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o[j][0] * inv, o[j][1 % OPL] * inv),
+                                                        pack_bf16x2(o[j][2 % OPL] * inv, o[j][3 % OPL] * inv));
+          } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[j][0] * inv, o[j][1 % OPL] * inv);
+          }
+          if (p.lse && lane == 0) p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = lse_v;
+        } else {
+          float* dst = p.ws_o + (static_cast<int64_t>(item) * p.heads + hq) * D + lane * OPL;
+#pragma unroll
+          for (int i = 0; i < OPL; ++i) dst[i] = o[j][i] * inv;
+          if (lane == 0) p.ws_lse[static_cast<int64_t>(item) * p.heads + hq] = lse_v;
+        }
+      }
+    }
+  }
+}
+
+// Combines the ranges of every multi-range row: one warp per (row, head).
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int OPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = static_cast<int64_t>(p.n_rows) * p.heads;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n;
+       w += wstride) {
+    const DecodeRow row = p.rows[w / p.heads];
+    const int hq = static_cast<int>(w % p.heads);
+    const int ns = (row.ctx + p.split_tokens - 1) / p.split_tokens;
+    if (ns <= 1) continue;
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32)
+      mx = fmaxf(mx, p.ws_lse[(static_cast<int64_t>(row.item0) + s) * p.heads + hq]);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+    float acc[OPL];
+#pragma unroll
+    for (int i = 0; i < OPL; ++i) acc[i] = 0.f;
+    float tot = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const int64_t it = static_cast<int64_t>(row.item0) + s;
+      const float wgt = __expf(p.ws_lse[it * p.heads + hq] - mx);
+      tot += wgt;
+      const float* src = p.ws_o + (it * p.heads + hq) * D + lane * OPL;
+#pragma unroll
+      for (int i = 0; i < OPL; ++i) acc[i] += wgt * src[i];
+    }
+    const float inv = 1.f / tot;
+    uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + lane * OPL;
+    if (OPL == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1 % OPL] * inv),
+                                                  pack_bf16x2(acc[2 % OPL] * inv, acc[3 % OPL] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % OPL] * inv);
+    }
+    if (p.lse && lane == 0) p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = mx + logf(tot);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t st) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  decode_kernel<D, G><<<items, 32 * (p.kv_heads + 1), kDecodeSmem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int grid = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(p.n_rows) * p.heads + 7) / 8,
+                                                static_cast<int64_t>(num_sms) * 16));
+  if (grid < 1) grid = 1;
+  decode_merge_kernel<D><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads) {
+  if (head_dim_qk != head_dim_v || (head_dim_qk != 64 && head_dim_qk != 128)) return false;
+  if (kv_heads < 1 || kv_heads > 8 || heads % kv_heads) return false;
+  const int g = heads / kv_heads;
+  // (128, 8) would hold 128 query values per lane and spill: the chunk kernel serves it.
+  return g == 1 || g == 2 || g == 4 || (g == 8 && head_dim_qk == 64);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, int num_sms,
+                          cudaStream_t stream) {
+  const int g = p.heads / p.kv_heads;
+  if (head_dim == 128) {
+    if (g == 1) return launch_t<128, 1>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<128, 2>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<128, 4>(p, items, num_sms, stream);
+  } else if (head_dim == 64) {
+    if (g == 1) return launch_t<64, 1>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<64, 2>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<64, 4>(p, items, num_sms, stream);
+    if (g == 8) return launch_t<64, 8>(p, items, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace vpp

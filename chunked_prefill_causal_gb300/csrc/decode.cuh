@@ -1,0 +1,51 @@
+// decode.cuh -- parameters of the split-KV decode kernel (shared with api.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace vpp {
+
+// One decode row of a mixed batch.
+struct DecodeRow {
+  int32_t b;      // sequence index (row of the block table)
+  int32_t q_row;  // packed query row in q/out
+  int32_t ctx;    // keys 0 .. ctx-1 (the row's own token included)
+  int32_t item0;  // first work item (key range) of this row
+};
+
+struct DecodeParams {
+  int32_t n_rows;
+  int32_t heads;
+  int32_t kv_heads;
+  int32_t split_tokens;        // keys per work item (multiple of 16)
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  float scale_log2;
+  int32_t pad0;
+  const uint16_t* q;           // bf16 [total_q][heads][d]
+  const uint16_t* k_cache;     // bf16 [num_blocks][64][kv_heads][d]
+  const uint16_t* v_cache;
+  const int32_t* block_table;  // [batch][max_blocks_per_seq]
+  uint16_t* out;               // bf16 [total_q][heads][d]
+  float* lse;                  // [heads][lse_stride], may be null
+  int64_t lse_stride;
+  float* ws_o;                 // float32 [items][heads][d] partials
+  float* ws_lse;               // [items][heads]
+  int* status;
+  DecodeRow rows[kMaxBatch];
+};
+
+// Keys per decode work item.
+constexpr int kDecodeSplitTokens = 1024;
+
+// True when the decode kernel handles this shape (dq = dv in {64, 128},
+// kv_heads <= 8, heads / kv_heads in {1, 2, 4}, or 8 when dq = 64).
+bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads);
+
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, int num_sms,
+                          cudaStream_t stream);
+
+}  // namespace vpp

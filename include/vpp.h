@@ -190,8 +190,11 @@ int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len,
  * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and its queries are its LAST
  * q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] positions: prefix
  * ctx_lens[b] - q_len_b.  ctx_lens[b] counts the sequence's own new tokens,
- * which must already be in the cache.  q_len_b == 1 is a decode row (split-KV
- * decode kernel); q_len_b > 1 is a prefill chunk (chunk-attention kernel);
+ * which must already be in the cache.  q_len_b == 1 is a decode row, served by
+ * the split-KV decode kernel (1024-key ranges merged through their LSE) when
+ * head_dim_qk == head_dim_v in {64, 128}, kv_heads <= 8 and heads/kv_heads is
+ * 1, 2 or 4 (or 8 with head dim 64), and by the chunk-attention kernel
+ * otherwise; q_len_b > 1 is a prefill chunk (chunk-attention kernel);
  * q_len_b == 0 is skipped.
  * cu_seqlens_q [batch+1] and ctx_lens [batch] are HOST int32 arrays (the
  * plan is built on the host and passed to the kernels by value; batch <=
