@@ -247,6 +247,113 @@ def workload_config(w):
             "exceed 129 MB)" if w.seq_len >= 32768 else "small inputs"}
 
 
+# ------------------------------------------------------------------ extras
+def time_events(fn, iters, stream):
+    """Median CUDA-event time (ms) of fn() over iters runs after one warm-up."""
+    fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+class MixedSetup:
+    """The mixed micro-batch resident in HBM: 4 prefill chunks + decode rows."""
+
+    def __init__(self, dev, decode_rows=None):
+        from chunked_prefill_causal_gb300 import vpp
+        m = W.MIXED if decode_rows is None else W.MixedWorkload(n_decode=decode_rows)
+        self.m = m
+        self.cu, self.ctx = m.batch()
+        q, ks, vs = W.mixed_tensors(m, dev)
+        table_np, pool = W.mixed_block_tables(m)
+        self.table = torch.from_numpy(table_np).to(dev)
+        self.kc = torch.zeros((pool, 64, m.kv_heads, m.head_dim_qk), dtype=torch.bfloat16, device=dev)
+        self.vc = torch.zeros((pool, 64, m.kv_heads, m.head_dim_v), dtype=torch.bfloat16, device=dev)
+        B = len(self.ctx)
+        for b in range(B):
+            P = int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b])
+            if P > 0:
+                vpp.vpp_kv_append(ks[b][:P], vs[b][:P], self.kc, self.vc, 0,
+                                  block_table=self.table[b].contiguous())
+        self.k_new = torch.cat([ks[b][int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b]):] for b in range(B)])
+        self.v_new = torch.cat([vs[b][int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b]):] for b in range(B)])
+        del ks, vs
+        self.q = q
+        self.out = torch.empty((int(self.cu[-1]), m.heads, m.head_dim_v), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((m.heads, int(self.cu[-1])), dtype=torch.float32, device=dev)
+        need = vpp.mixed_attn_workspace_size(self.cu, self.ctx, m.heads, m.kv_heads, m.head_dim_qk,
+                                             m.head_dim_v)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        n_pre = len(m.prefill_prefixes)
+        self.prefill_flops = sum(2.0 * (m.head_dim_qk + m.head_dim_v) * m.heads
+                                 * (m.prefill_chunk * p + m.prefill_chunk * (m.prefill_chunk + 1) // 2)
+                                 for p in m.prefill_prefixes)
+        self.decode_flops = sum(2.0 * (m.head_dim_qk + m.head_dim_v) * m.heads * int(c)
+                                for c in self.ctx[n_pre:])
+        self.decode_bytes = sum(int(c) for c in self.ctx[n_pre:]) * m.kv_heads * (
+            m.head_dim_qk + m.head_dim_v) * 2
+        # The decode rows alone, as their own batch.
+        self.cu_d = np.arange(B - n_pre + 1, dtype=np.int32)
+        self.ctx_d = self.ctx[n_pre:].copy()
+        self.q_d = q[int(self.cu[n_pre]):].contiguous()
+        self.table_d = self.table[n_pre:].contiguous()
+        self.out_d = torch.empty((B - n_pre, m.heads, m.head_dim_v), dtype=torch.bfloat16, device=dev)
+        need_d = vpp.mixed_attn_workspace_size(self.cu_d, self.ctx_d, m.heads, m.kv_heads, m.head_dim_qk,
+                                               m.head_dim_v)
+        self.ws_d = torch.empty(max(need_d, 256), dtype=torch.uint8, device=dev)
+
+    def step(self):
+        from chunked_prefill_causal_gb300 import vpp
+        vpp.vpp_kv_append_varlen(self.k_new, self.v_new, self.kc, self.vc, self.table, self.cu, self.ctx)
+        vpp.vpp_mixed_attn(self.q, self.kc, self.vc, self.table, self.cu, self.ctx, out=self.out,
+                           lse=self.lse, workspace=self.ws)
+
+    def decode_only(self):
+        from chunked_prefill_causal_gb300 import vpp
+        vpp.vpp_mixed_attn(self.q_d, self.kc, self.vc, self.table_d, self.cu_d, self.ctx_d,
+                           out=self.out_d, workspace=self.ws_d)
+
+
+def measure_mixed(dev, stream, hbm, peak_tf, decode_rows=None):
+    ms = MixedSetup(dev, decode_rows)
+    step_ms = time_events(ms.step, 10, stream)
+    dec_ms = time_events(ms.decode_only, 10, stream)
+    gbs = ms.decode_bytes / (dec_ms / 1e3) / 1e9
+    return {"workload": "mixed: 4 prefill chunks of 2048 at prefixes {0,16384,65536,122880} + "
+                        f"{len(ms.ctx_d)} decode rows, ctx ~ U[1024,32768]; 32/8 heads, d 128",
+            "step_ms": round(step_ms, 3),
+            "decode_only_ms": round(dec_ms, 3),
+            "decode_bytes": int(ms.decode_bytes),
+            "decode_gbs": round(gbs, 1), "decode_frac_hbm": round(gbs / hbm, 4),
+            "prefill_plus_decode_tflops": round((ms.prefill_flops + ms.decode_flops) / (step_ms / 1e3) / 1e12, 1),
+            "launches_per_step": 4}
+
+
+def measure_append(dev, stream, hbm):
+    """One MLA-chunk-sized append: 24576 tokens x 128 kv heads x (192 + 128) bf16."""
+    from chunked_prefill_causal_gb300 import vpp
+    C, H, dq, dv = 24576, 128, 192, 128
+    g = torch.Generator(device=dev).manual_seed(77)
+    k = torch.randn((C, H, dq), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((C, H, dv), generator=g, device=dev).to(torch.bfloat16)
+    nb = C // 64 + 8
+    table = torch.from_numpy(W.block_table(C // 64, nb, 5)).to(dev)
+    kc = torch.empty((nb, 64, H, dq), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty((nb, 64, H, dv), dtype=torch.bfloat16, device=dev)
+    t = time_events(lambda: vpp.vpp_kv_append(k, v, kc, vc, 0, block_table=table), 10, stream)
+    byts = 2 * C * H * (dq + dv) * 2
+    return {"tokens": C, "kv_heads": H, "head_dims": [dq, dv], "bytes_moved": byts, "ms": round(t, 4),
+            "gbs": round(byts / (t / 1e3) / 1e9, 1), "frac_hbm": round(byts / (t / 1e3) / 1e9 / hbm, 4)}
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist_):
     from chunked_prefill_causal_gb300 import vpp
@@ -411,6 +518,13 @@ def run_ours(args, dist_):
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": desc}
 
+    extras = {}
+    if not args.no_extras:
+        del qs, ks, vs
+        torch.cuda.empty_cache()
+        extras["kv_append"] = measure_append(dev, stream, hbm)
+        extras["mixed"] = measure_mixed(dev, stream, hbm, peak_tf)
+
     if dist_.rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist_.world,
@@ -434,7 +548,51 @@ def run_ours(args, dist_):
             "kv_append_bytes_per_step": int(sum(app_bytes)),
             "hbm_peak_gbs": hbm,
         }
+        line.update(extras)
         print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_mixed(args, dist_):
+    """The mixed micro-batch as the step: varlen append of the batch's new
+    tokens, then vpp_mixed_attn (prefill chunks + split-KV decode rows)."""
+    from chunked_prefill_causal_gb300 import vpp
+
+    dist_.init()
+    dev = torch.device("cuda", dist_.local)
+    torch.cuda.set_device(dev)
+    vpp.load()
+    pk, pk_src = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    stream = torch.cuda.current_stream()
+    ms = MixedSetup(dev, args.decode_rows)
+    for _ in range(args.warmup):
+        ms.step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dist_.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        ms.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist_.barrier()
+    if vpp.vpp_last_device_status() != 0:
+        raise RuntimeError("device status word reported an error")
+    el = dist_.max(e0.elapsed_time(e1) / 1e3)
+    dec_ms = time_events(ms.decode_only, 5, stream)
+    gbs = ms.decode_bytes / (dec_ms / 1e3) / 1e9
+    if dist_.rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": (ms.prefill_flops + ms.decode_flops) * args.steps * dist_.world / el / 1e12,
+            "unit": "TFLOP/s", "n_gpus": dist_.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "mixed", "decode_rows": len(ms.ctx_d), "heads": 32, "kv_heads": 8,
+                       "head_dim": 128},
+            "decode_only_ms": round(dec_ms, 3), "decode_gbs": round(gbs, 1),
+            "decode_frac_hbm": round(gbs / hbm, 4), "hbm_peak_source": pk_src}), flush=True)
     return 0
 
 
@@ -444,9 +602,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="long128k")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + ["mixed"], default="long128k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the KV-append and mixed-batch measurements")
+    ap.add_argument("--decode-rows", type=int, default=None,
+                    help="with --workload mixed: decode rows of the micro-batch (default 256)")
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=256)
@@ -456,7 +618,11 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     dist_ = Dist()
     if args.impl == "reference":
+        if args.workload == "mixed":
+            args.workload = "long128k"
         return run_reference(args, dist_)
+    if args.workload == "mixed":
+        return run_mixed(args, dist_)
     return run_ours(args, dist_)
 
 
