@@ -51,17 +51,15 @@ constexpr int kSmemLimit = 232448; // 227 KB per CTA on sm_103a
 constexpr int kSubTileBytes = kTileN * 64 * 2;  // 128 keys x 64 bf16 (one 128B-swizzled block)
 
 __host__ __device__ constexpr int attn_q_bytes(int dq) { return 2 * (dq / 64) * kSubTileBytes; }
-// A ring stage holds one K tile or one V tile: max(dq, dv) / 64 sub-tiles.
-__host__ __device__ constexpr int attn_stage_bytes(int dq, int dv) {
-  return (dq > dv ? dq : dv) / 64 * kSubTileBytes;
-}
-__host__ __device__ constexpr int attn_num_stages(int dq, int dv) {
-  return (kSmemLimit - attn_q_bytes(dq) - 2048) / attn_stage_bytes(dq, dv) > 8
-             ? 8
-             : (kSmemLimit - attn_q_bytes(dq) - 2048) / attn_stage_bytes(dq, dv);
+// The K/V ring is made of 16 KB sub-tile slots (128 keys x 64 dims); a K tile
+// takes dq/64 consecutive slots and a V tile dv/64 (modulo the ring size).
+__host__ __device__ constexpr int attn_num_slots(int dq) {
+  return (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes > 12
+             ? 12
+             : (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes;
 }
 __host__ __device__ constexpr int attn_smem_bytes(int dq, int dv) {
-  return 1024 + attn_q_bytes(dq) + attn_num_stages(dq, dv) * attn_stage_bytes(dq, dv) + 1024;
+  return 1024 + attn_q_bytes(dq) + attn_num_slots(dq) * kSubTileBytes + 1024 + 0 * dv;
 }
 
 cudaError_t launch_chunk_attn(int dq, int dv, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -15,8 +15,11 @@
 //
 // CTA shape (384 threads, one CTA per SM):
 //   warp 0      TMA producer: the CTA's two 128-row query tiles once, then K
-//               and V tiles through a ring of shared-memory stages (one stage
-//               = one K tile or one V tile, one full/empty mbarrier pair).
+//               and V tiles through a ring of 16 KB shared-memory slots (128
+//               keys x 64 dims each).  A K tile takes dq/64 consecutive slots
+//               and a V tile dv/64 (wrapping at the ring's end); each tile has
+//               one full and one empty mbarrier, and slots are reused in order
+//               as tiles are released.
 //   warp 1, 3   MMA issuers, one elected lane each: warp 1 for query tile A,
 //               warp 3 for tile B.  S = Q K^T into TMEM (kind::f16, bf16 in,
 //               f32 accumulate), then O += P V with P read from TMEM.  Each
@@ -71,16 +74,23 @@ template <int DQ, int DV>
 struct Shape {
   static constexpr int NQC = DQ / 64;  // 64-dim sub-tiles of a K tile (and of Q)
   static constexpr int NVC = DV / 64;  // 64-dim sub-tiles of a V tile
-  static constexpr int NSTAGE = attn_num_stages(DQ, DV);
-  static constexpr int STAGE_BYTES = attn_stage_bytes(DQ, DV);
+  static constexpr int NSLOT = attn_num_slots(DQ);
+  static constexpr int NB = NSLOT;     // tile barriers (>= tiles that fit the ring)
   static constexpr int QBYTES = attn_q_bytes(DQ);
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kTileN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, DV, false, true);
-  // barrier indices: Q, S[2], P[2], O[2], FINAL[2], TMP, FULL[NSTAGE], EMPTY[NSTAGE]
+  static constexpr uint32_t IDESC_PV64 = idesc_bf16_f32(kTileM, 64, false, true);
+  // barrier indices: Q, S[2], P[2], O[2], FINAL[2], TMP, FULL[NB], EMPTY[NB]
   static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_FULL = 10,
-                       B_EMPTY = 10 + NSTAGE, NBARS = 10 + 2 * NSTAGE;
-  static_assert(NSTAGE >= 2, "ring must hold one K and one V tile");
+                       B_EMPTY = 10 + NB, NBARS = 10 + 2 * NB;
+  static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
   static_assert(DV <= 128, "O accumulators must fit TMEM next to two S tiles");
+  // Tile t of the load order (K_0, V_0, K_1, V_1, ...) starts at ring position
+  // tile_pos(t) (counted in slots from the first tile, not wrapped).
+  __device__ __forceinline__ static int tile_pos(int t) {
+    return (t >> 1) * (NQC + NVC) + ((t & 1) ? NQC : 0);
+  }
+  __device__ __forceinline__ static int tile_slots(int t) { return (t & 1) ? NVC : NQC; }
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status,
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + S::QBYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSTAGE * S::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSLOT * kSubTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
   volatile int* turn = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -145,7 +155,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(S::B_FINAL + x), 1);
     }
     mbar_init(bar(S::B_TMP), 1);
-    for (int i = 0; i < S::NSTAGE; ++i) {
+    for (int i = 0; i < S::NB; ++i) {
       mbar_init(bar(S::B_FULL + i), 1);
       mbar_init(bar(S::B_EMPTY + i), 2);  // released by both MMA issuers
     }
@@ -176,9 +186,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < S::NQC; ++c)
           tma_load_4d(smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes), &tm_q, bar(S::B_Q),
                       c * 64, 0, g, seg.q_start + tok0 + x * T);
-      Ring r{0, 0u};
-      uint32_t filled = 0u, fill_phase = 0u;
       bool ok = true;
+      int issued = 0;  // tiles whose loads were started
+      int rq = 0;      // next tile whose release has not been observed
       auto block_coord = [&](int b) -> int {
         if (b * kBlockTokens >= seg.kv_len) return p.num_blocks;  // reads zeros
         const int e = p.block_table[seg.table_off + b];
@@ -188,11 +198,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return e;
       };
-      // Loads nsub sub-tiles (two 64-key blocks each) of K or V into a stage.
-      auto load_part = [&](const CUtensorMap* m, int nsub, uint32_t dst, uint32_t fb, int c0,
-                           int c1) {
+      // Loads the nsub sub-tiles (two 64-key blocks each) of tile t.
+      auto load_tile = [&](const CUtensorMap* m, int nsub, int pos, uint32_t fb, int c0, int c1) {
         for (int c = 0; c < nsub; ++c) {
-          const uint32_t d = dst + c * kSubTileBytes;
+          const uint32_t d = smem_u32(sRing + ((pos + c) % S::NSLOT) * kSubTileBytes);
           if (p.paged) {
             tma_load_4d(d, m, fb, c * 64, g, 0, c0);
             tma_load_4d(d + kSubTileBytes / 2, m, fb, c * 64, g, 0, c1);
@@ -213,26 +222,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c1 = key0 + kBlockTokens;
         }
         for (int part = 0; part < 2; ++part) {  // K, then V
-          if (!mbar_wait(bar(S::B_EMPTY + r.slot), r.phase ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
+          const int t = 2 * j + part;
+          const int pos = S::tile_pos(t);
+          const int nsub = S::tile_slots(t);
+          // Tiles are released in load order: wait until every tile that used
+          // these slots, and the tile that last used this barrier, is released.
+          while (rq < t && (rq <= t - S::NB || S::tile_pos(rq) < pos + nsub - S::NSLOT)) {
+            if (!mbar_wait(bar(S::B_EMPTY + rq % S::NB), (rq / S::NB) & 1u, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ++rq;
           }
-          const uint32_t dst = smem_u32(sRing + r.slot * S::STAGE_BYTES);
-          const uint32_t fb = bar(S::B_FULL + r.slot);
-          const int nsub = part == 0 ? S::NQC : S::NVC;
+          if (!ok) break;
+          const uint32_t fb = bar(S::B_FULL + t % S::NB);
           const CUtensorMap* m = part == 0 ? &tm_k : &tm_v;
           // Rows of the last loaded block at positions >= kv_len hold whatever
-          // the pool holds there; their V rows are zeroed before the stage is
+          // the pool holds there; their V rows are zeroed before the tile is
           // released so that P = 0 times them stays 0 (K rows there are masked
           // to -inf before the softmax).  This happens at most once per CTA.
           const int r0 = seg.kv_len - key0;
           const bool fix = part == 1 && p.paged && r0 > 0 && r0 < kTileN && (r0 % kBlockTokens) != 0;
           if (!fix) {
             mbar_arrive_expect_tx(fb, nsub * kSubTileBytes);
-            load_part(m, nsub, dst, fb, c0, c1);
+            load_tile(m, nsub, pos, fb, c0, c1);
           } else {
             mbar_arrive_expect_tx(bar(S::B_TMP), nsub * kSubTileBytes);
-            load_part(m, nsub, dst, bar(S::B_TMP), c0, c1);
+            load_tile(m, nsub, pos, bar(S::B_TMP), c0, c1);
             if (!mbar_wait(bar(S::B_TMP), 0, p.status, abort_flag)) {
               mbar_wait_for(bar(S::B_TMP), 0, kCleanupNs);
               ok = false;
@@ -242,23 +258,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
             for (int c = 0; c < nsub; ++c)
               for (int row = r0; row < r1; ++row) {
-                uint4* rp = reinterpret_cast<uint4*>(sRing + r.slot * S::STAGE_BYTES +
-                                                     c * kSubTileBytes + row * 128);
+                uint4* rp = reinterpret_cast<uint4*>(sRing + ((pos + c) % S::NSLOT) * kSubTileBytes +
+                                                     row * 128);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) rp[u] = z;
               }
             fence_proxy_async_smem();
             mbar_arrive(fb);
           }
-          filled |= 1u << r.slot;
-          fill_phase = (fill_phase & ~(1u << r.slot)) | (r.phase << r.slot);
-          r.advance(S::NSTAGE);
+          ++issued;
         }
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA exits.
-        for (int i = 0; i < S::NSTAGE; ++i)
-          if (filled & (1u << i)) mbar_wait_for(bar(S::B_FULL + i), (fill_phase >> i) & 1u, kCleanupNs);
+        for (int t = issued > S::NB ? issued - S::NB : 0; t < issued; ++t)
+          mbar_wait_for(bar(S::B_FULL + t % S::NB), (t / S::NB) & 1u, kCleanupNs);
         mbar_wait_for(bar(S::B_Q), 0, kCleanupNs);
       }
     } else if ((warp == 1 || warp == 3) && lane == 0) {
@@ -271,32 +285,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t dk0 = sdesc_sw128(smem_u32(sRing), 16, 1024);             // K-major
       const uint64_t dv0 = sdesc_sw128(smem_u32(sRing), kSubTileBytes, 1024);  // MN-major
       constexpr uint32_t kSub16 = kSubTileBytes >> 4;
-      constexpr uint32_t kStage16 = S::STAGE_BYTES >> 4;
       const uint32_t tS = tbase + x * kTileN;
       const uint32_t tO = tbase + 2 * kTileN + x * DV;
-      Ring r{0, 0u};
-      int pvs = 0;          // stage of V(j-1)
-      uint32_t pvph = 0u;
       bool ok = mbar_wait(bar(S::B_Q), 0, p.status, abort_flag);
+      // Ring slots of K_j and V_{j-1}, advanced by one tile pair per block.
+      int kslot = 0;
+      int vslot = S::NQC - (S::NQC + S::NVC);  // becomes V_0's slot at j = 1
+      if (vslot < 0) vslot += S::NSLOT;
       // Block j = [PV(x, j-1) if j > 0][QK(x, j) if j < n_kv]; blocks run in
       // the global order A0 B0 A1 B1 ...: block j of issuer x is number 2j+x.
       for (int j = 0; ok && j <= n_kv; ++j) {
-        int ks = 0, vs = 0;
-        uint32_t kph = 0u, vph = 0u;
-        if (j < n_kv) {
-          ks = r.slot;
-          kph = r.phase;
-          r.advance(S::NSTAGE);
-          vs = r.slot;
-          vph = r.phase;
-          r.advance(S::NSTAGE);
+        const int tk = 2 * j;      // tile index of K_j
+        const int tv = 2 * j - 1;  // tile index of V_{j-1}
+        if (j > 0) {
+          kslot += S::NQC + S::NVC;
+          if (kslot >= S::NSLOT) kslot -= S::NSLOT;
+          vslot += S::NQC + S::NVC;
+          if (vslot >= S::NSLOT) vslot -= S::NSLOT;
         }
         if (j > 0) {
-          if (!(ok = mbar_wait(bar(S::B_FULL + pvs), pvph, p.status, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(S::B_FULL + tv % S::NB), (tv / S::NB) & 1u, p.status, abort_flag))) break;
           if (!(ok = mbar_wait(bar(S::B_P + x), (j - 1) & 1, p.status, abort_flag))) break;
           tc_fence_after();
         }
-        if (j < n_kv && !(ok = mbar_wait(bar(S::B_FULL + ks), kph, p.status, abort_flag))) break;
+        if (j < n_kv &&
+            !(ok = mbar_wait(bar(S::B_FULL + tk % S::NB), (tk / S::NB) & 1u, p.status, abort_flag)))
+          break;
         // Take the turn (bounded spin; gives up if another role aborted).
         if (*turn != 2 * j + x) {
           const uint64_t t0 = globaltimer_ns();
@@ -313,31 +327,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (j > 0) {
           // O += P V for tile j-1 (P read from TMEM, V from the ring).
-          const uint64_t vb = dv0 + pvs * kStage16;
+          if (S::NVC == 1 || vslot + S::NVC <= S::NSLOT) {
+            // Adjacent V sub-tiles: one N = DV chain (LBO = one sub-tile).
+            const uint64_t vb = dv0 + vslot * kSub16;
 #pragma unroll
-          for (int k = 0; k < kTileN / 16; ++k)
-            umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 1 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kTileN / 16; ++k)
+              umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 1 || k > 0) ? 1u : 0u);
+          } else {
+            // The V tile wraps around the ring: one N = 64 chain per sub-tile.
+#pragma unroll
+            for (int h = 0; h < S::NVC; ++h) {
+              const int vs = vslot + h < S::NSLOT ? vslot + h : vslot + h - S::NSLOT;
+              const uint64_t vb = dv0 + vs * kSub16;
+#pragma unroll
+              for (int k = 0; k < kTileN / 16; ++k)
+                umma_ts(tO + 64 * h, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV64,
+                        (j > 1 || k > 0) ? 1u : 0u);
+            }
+          }
         }
         if (j < n_kv) {
           // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
           // same TMEM columns, in issue order.
-          const uint64_t kb = dk0 + ks * kStage16;
 #pragma unroll
-          for (int c = 0; c < S::NQC; ++c)
+          for (int c = 0; c < S::NQC; ++c) {
+            const int ks = kslot + c < S::NSLOT ? kslot + c : kslot + c - S::NSLOT;
+            const uint64_t kb = dk0 + ks * kSub16;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + c * kSub16 + 2 * k, S::IDESC_QK,
-                      (c | k) ? 1u : 0u);
+              umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + 2 * k, S::IDESC_QK, (c | k) ? 1u : 0u);
+          }
         }
         *turn = 2 * j + x + 1;
         if (j < n_kv) {
           umma_commit(bar(S::B_S + x));
-          umma_commit(bar(S::B_EMPTY + ks));
+          umma_commit(bar(S::B_EMPTY + tk % S::NB));
         }
-        if (j > 0) umma_commit(bar(S::B_EMPTY + pvs));
+        if (j > 0) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         if (j == n_kv) umma_commit(bar(S::B_O + x));
-        pvs = vs;
-        pvph = vph;
       }
       if (!ok) {
         *abort_flag = 1u;  // the partner issuer may be waiting for this turn
