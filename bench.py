@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture
 # (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "7c36a21a363d67e387c1560676e33157d7e5f4a5895506d79c3fd4fb61441c62", "bytes_per_launch": 1.2117e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "c73c363cc8d6275114598861f18e2167f23b5058a06fa51be9b50d3d44466b8b", "bytes_per_launch": 1.2134e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 
@@ -478,35 +478,64 @@ def run_ours(args, dist_):
         hv = [v.to("cpu").pin_memory() for v in vs]
         ho = torch.empty((len(chunks), Cmax, w.heads, w.head_dim_v), dtype=torch.bfloat16).pin_memory()
         hl = torch.empty((len(chunks), w.heads, Cmax), dtype=torch.float32).pin_memory()
-        dq_ = torch.empty_like(qs[0])
-        dk_ = torch.empty_like(ks[0])
-        dv_ = torch.empty_like(vs[0])
-        lse_e = torch.empty((w.heads, Cmax), dtype=torch.float32, device=dev)
+        # Double-buffered pipeline: chunk k+1's inputs are copied in (h2d
+        # stream) and chunk k-1's results copied out (d2h stream) while chunk k
+        # runs on the compute stream; events order the reuse of each buffer.
+        dq2 = [torch.empty_like(qs[0]) for _ in range(2)]
+        dk2 = [torch.empty_like(ks[0]) for _ in range(2)]
+        dv2 = [torch.empty_like(vs[0]) for _ in range(2)]
+        do2 = [torch.empty((Cmax, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        dl2 = [torch.empty((w.heads, Cmax), dtype=torch.float32, device=dev) for _ in range(2)]
+        h2d_s = torch.cuda.Stream(device=dev)
+        d2h_s = torch.cuda.Stream(device=dev)
         h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
         d2h = sum(C * w.heads * w.head_dim_v * 2 + w.heads * C * 4 for _, C in chunks)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        state = {"first": True}
 
         def e2e_step():
             for ci, (P, C) in enumerate(chunks):
-                dq_[:C].copy_(hq[ci], non_blocking=True)
-                dk_[:C].copy_(hk[ci], non_blocking=True)
-                dv_[:C].copy_(hv[ci], non_blocking=True)
-                vpp.vpp_kv_append(dk_[:C], dv_[:C], kc, vc, P, block_table=table)
-                o = vpp.vpp_chunk_attn_ex(dq_[:C], kc, vc, P, block_table=table, out=out[:C],
-                                          lse=lse_e[:, :C] if C == Cmax else None, workspace=ws)
-                ho[ci, :C].copy_(o, non_blocking=True)
-                hl[ci].copy_(lse_e, non_blocking=True)
+                b = ci & 1
+                with torch.cuda.stream(h2d_s):
+                    if not state["first"] or ci >= 2:
+                        h2d_s.wait_event(ev_comp[b])     # the compute that read buffer b is done
+                    dq2[b][:C].copy_(hq[ci], non_blocking=True)
+                    dk2[b][:C].copy_(hk[ci], non_blocking=True)
+                    dv2[b][:C].copy_(hv[ci], non_blocking=True)
+                    ev_in[b].record(h2d_s)
+                stream.wait_event(ev_in[b])
+                if not state["first"] or ci >= 2:
+                    stream.wait_event(ev_out[b])         # out/lse of buffer b were copied back
+                vpp.vpp_kv_append(dk2[b][:C], dv2[b][:C], kc, vc, P, block_table=table)
+                vpp.vpp_chunk_attn_ex(dq2[b][:C], kc, vc, P, block_table=table, out=do2[b][:C],
+                                      lse=dl2[b] if C == Cmax else None, workspace=ws)
+                ev_comp[b].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(ev_comp[b])
+                    ho[ci, :C].copy_(do2[b][:C], non_blocking=True)
+                    hl[ci].copy_(dl2[b], non_blocking=True)
+                    ev_out[b].record(d2h_s)
+            state["first"] = False
 
         e2e_step()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         dist_.barrier()
+        torch.cuda.synchronize()
+        t_host0 = time.perf_counter()
         e0.record(stream)
+        h2d_s.wait_stream(stream)
+        d2h_s.wait_stream(stream)
         for _ in range(args.steps):
             e2e_step()
+        stream.wait_stream(d2h_s)
+        stream.wait_stream(h2d_s)
         e1.record(stream)
         torch.cuda.synchronize()
-        et = dist_.max(e0.elapsed_time(e1) / 1e3)
+        et = dist_.max(max(e0.elapsed_time(e1) / 1e3, time.perf_counter() - t_host0))
         e2e = {"value": sum(flops) * args.steps * dist_.world / et / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * et / args.steps}
