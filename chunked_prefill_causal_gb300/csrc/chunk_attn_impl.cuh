@@ -405,20 +405,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (key0 + c > lim) sv[c] = -INFINITY;
       }
-      // Row max: eight independent chains of 3-input max, then a tree.
-      float mx8[8];
+      // Row max (eight independent chains of 3-input max, then a tree).
+      auto row_max = [&]() {
+        float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-      for (int c = 8; c < 128; c += 16)
+        for (int c = 8; c < 128; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
-      const float m_new = fmaxf(m, mx * sl);
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+        return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                     fmaxf(mx8[6], mx8[7]));
+      };
+      // p = 2^(s * scale * log2(e) - mref), two lanes of work per packed FMA,
+      // stored to TMEM in two halves (the first store overlaps the second
+      // half's exponentials); returns the row sum of p.
+      auto exps_to_tmem = [&](float mref) -> float {
+        const float mb = (mref == -INFINITY) ? 0.f : mref;
+        const float2 sl2 = make_float2(sl, sl);
+        const float2 nmb2 = make_float2(-mb, -mb);
+        float2 rs4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
+        uint32_t pk0[32], pk1[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
+          const float a = ex2_approx(xx.x);
+          const float b = ex2_approx(xx.y);
+          rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
+          pk0[c] = pack_bf16x2(a, b);
+        }
+        tmem_st32(tS, pk0);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 xx = ffma2(make_float2(sv[64 + 2 * c], sv[64 + 2 * c + 1]), sl2, nmb2);
+          const float a = ex2_approx(xx.x);
+          const float b = ex2_approx(xx.y);
+          rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
+          pk1[c] = pack_bf16x2(a, b);
+        }
+        tmem_st32(tS + 32, pk1);
+        const float2 rs2 = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
+        return rs2.x + rs2.y;
+      };
+      float rs;
       if (j == 0) {
-        m = m_new;
+        m = row_max() * sl;
+        rs = exps_to_tmem(m);
       } else {
+        // The exponentials use the running max right away and the row max is
+        // computed alongside, off the critical path.  Only when it has grown
+        // by more than 2^8 are O and the denominator rescaled and the
+        // exponentials redone (rare after the first tile; the result is exact
+        // either way since numerator and denominator share the reference m).
+        rs = exps_to_tmem(m);
+        const float m_new = fmaxf(m, row_max() * sl);
         const bool need = m_new > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           // O of this tile is idle here: PV(x, j-1) completed before S(x, j)
@@ -428,6 +470,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l *= f;
             m = m_new;
           }
+          tmem_st_wait();
 #pragma unroll
           for (int q = 0; q < DV / 32; ++q) {
             uint32_t o[32];
@@ -438,41 +481,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tmem_st32(tO + 32 * q, o);
           }
           tmem_st_wait();
+          rs = exps_to_tmem(m);  // rows whose m did not move rewrite the same values
         }
       }
-      // p = 2^(s * scale * log2(e) - m), two lanes of work per packed FMA;
-      // P is stored to TMEM in two halves so the first store overlaps the
-      // second half's exponentials.
-      const float mb = (m == -INFINITY) ? 0.f : m;
-      const float2 sl2 = make_float2(sl, sl);
-      const float2 nmb2 = make_float2(-mb, -mb);
-      float2 rs4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
-      uint32_t pk0[32], pk1[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
-        const float a = ex2_approx(xx.x);
-        const float b = ex2_approx(xx.y);
-        rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
-        pk0[c] = pack_bf16x2(a, b);
-      }
-      tmem_st32(tS, pk0);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 xx = ffma2(make_float2(sv[64 + 2 * c], sv[64 + 2 * c + 1]), sl2, nmb2);
-        const float a = ex2_approx(xx.x);
-        const float b = ex2_approx(xx.y);
-        rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
-        pk1[c] = pack_bf16x2(a, b);
-      }
-      tmem_st32(tS + 32, pk1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(S::B_P + x));
-      const float2 rs2 = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
-      l += rs2.x + rs2.y;
+      l += rs;
     }
     if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);
     if (ok) {
