@@ -354,6 +354,65 @@ def measure_append(dev, stream, hbm):
             "gbs": round(byts / (t / 1e3) / 1e9, 1), "frac_hbm": round(byts / (t / 1e3) / 1e9 / hbm, 4)}
 
 
+def measure_cost_model(dev, stream, n_batches=48, n_train=32, seed=11):
+    """Times random mixed micro-batches through vpp_mixed_attn and fits the
+    micro-batch latency model (cost_model.py) to them: MAPE on held-out
+    batches for the full model and for token counts alone, and the error of
+    the online (RLS) predictions."""
+    from chunked_prefill_causal_gb300 import vpp
+    from chunked_prefill_causal_gb300.cost_model import LatencyModel, MicroBatch, mape
+    H, Hkv, d = 32, 8, 128
+    rng = np.random.default_rng(seed)
+    specs = []
+    for _ in range(n_batches):
+        pre = [(int(rng.integers(0, 1536)) * 64, int(rng.choice([256, 512, 1024, 2048, 4096])))
+               for _ in range(int(rng.integers(0, 4)))]
+        dec = [int(x) for x in rng.integers(1024, 32769, size=int(rng.integers(0, 129)))]
+        if not pre and not dec:
+            dec = [4096]
+        specs.append(MicroBatch(tuple(pre), tuple(dec)))
+    max_tokens = max(sum(p + c for p, c in b.prefill) + sum(b.decode) for b in specs)
+    pool = W.blocks_for(max_tokens) + 512
+    kc = torch.zeros((pool, 64, Hkv, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    times = []
+    for b in specs:
+        qlen = [c for _, c in b.prefill] + [1] * len(b.decode)
+        ctx = [p + c for p, c in b.prefill] + list(b.decode)
+        cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+        ctx = np.asarray(ctx, dtype=np.int32)
+        need = [W.blocks_for(int(c)) for c in ctx]
+        table = np.zeros((len(ctx), max(need)), dtype=np.int32)
+        off = 0
+        for i, n in enumerate(need):
+            table[i, :n] = np.arange(off, off + n)
+            off += n
+        table_d = torch.from_numpy(table).to(dev)
+        q = torch.randn((int(cu[-1]), H, d), device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        wsz = vpp.mixed_attn_workspace_size(cu, ctx, H, Hkv, d, d)
+        ws = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+        t = time_events(lambda: vpp.vpp_mixed_attn(q, kc, vc, table_d, cu, ctx, out=out, workspace=ws), 5, stream)
+        times.append(t)
+    tr, te = slice(0, n_train), slice(n_train, n_batches)
+    full = LatencyModel()
+    full.fit_all(specs[tr], times[tr])
+    tok = LatencyModel()
+    tok.fit_offline(specs[tr], times[tr])
+    online = LatencyModel(forgetting=0.98)
+    online.alpha = tok.alpha.copy()
+    online_pred = [online.update(b, t) for b, t in zip(specs, times)]
+    return {"batches": n_batches, "train": n_train,
+            "heldout_mape_full": round(mape([full.predict(b) for b in specs[te]], times[te]), 4),
+            "heldout_mape_tokens_only": round(mape([tok.predict(b) for b in specs[te]], times[te]), 4),
+            "online_rls_mape_last16": round(mape(online_pred[-16:], times[-16:]), 4),
+            "coefficients_ms": {"alpha": [round(float(x), 6) for x in full.alpha],
+                                "beta": [round(float(x), 6) for x in full.beta],
+                                "units": "alpha: [1, N/2^10]; beta: [sum Lpast*Lpre/2^30, sum Lpre^2/2^30, "
+                                         "sum Ldec/2^20]"},
+            "latency_ms_range": [round(min(times), 3), round(max(times), 3)]}
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist_):
     from chunked_prefill_causal_gb300 import vpp
@@ -553,6 +612,8 @@ def run_ours(args, dist_):
         torch.cuda.empty_cache()
         extras["kv_append"] = measure_append(dev, stream, hbm)
         extras["mixed"] = measure_mixed(dev, stream, hbm, peak_tf)
+        torch.cuda.empty_cache()
+        extras["cost_model"] = measure_cost_model(dev, stream)
 
     if dist_.rank == 0:
         line = {
