@@ -413,6 +413,34 @@ def measure_cost_model(dev, stream, n_batches=48, n_train=32, seed=11):
             "latency_ms_range": [round(min(times), 3), round(max(times), 3)]}
 
 
+def schedule_summary(tau_ms):
+    """Two-rank CPP vs V-shaped VPP vs VPP with pipelined packing, simulated
+    on the measured per-chunk attention latencies tau_k (one layer, ms): a
+    stage's time scales with its layer count, which leaves every ratio as is."""
+    from chunked_prefill_causal_gb300 import schedule_sim as S
+    n = len(tau_ms)
+    c, v = S.cpp(tau_ms), S.vpp(tau_ms)
+    two_plain = S.vpp_requests([tau_ms, tau_ms])
+    two_packed = S.vpp_requests([tau_ms, tau_ms], pack=True)
+    two_cpp = S.cpp_requests([tau_ms, tau_ms])
+    packed, _ = S.pack_leading_chunks(S.drain_window_from_taus(tau_ms), tau_ms) if n > 1 else (0, 0.0)
+    eq3b = [abs(tau_ms[k - 1] + tau_ms[k + 1] - 2 * tau_ms[k]) / (2 * tau_ms[k]) for k in range(1, n - 1)]
+    r = lambda x: round(float(x), 4)
+    return {"chunks": n, "tau_ms": [r(t) for t in tau_ms],
+            "eq3b_max_rel_residual": r(max(eq3b)) if eq3b else None,
+            "boundary_tau1_over_2tau0": r(tau_ms[1] / (2 * tau_ms[0])) if n > 1 else None,
+            "cpp_ms": r(c.makespan), "vpp_ms": r(v.makespan), "vpp_speedup": r(c.makespan / v.makespan),
+            "cpp_bubble_ratio": r(c.bubble_ratio), "vpp_bubble_ratio": r(v.bubble_ratio),
+            "drain_idle_ms": r(S.drain_idle(v, 0, n)) if n > 1 else None,
+            "drain_estimate_ms": r(S.drain_window_from_taus(tau_ms)) if n > 1 else None,
+            "drain_estimate_eq2_ms": r(S.drain_window(n, tau_ms[0])),
+            "two_requests": {"cpp_ms": r(two_cpp.makespan), "vpp_ms": r(two_plain.makespan),
+                             "vpp_packed_ms": r(two_packed.makespan), "packed_chunks": packed,
+                             "cpp_bubble_ratio": r(two_cpp.bubble_ratio),
+                             "vpp_bubble_ratio": r(two_plain.bubble_ratio),
+                             "vpp_packed_bubble_ratio": r(two_packed.bubble_ratio)}}
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist_):
     from chunked_prefill_causal_gb300 import vpp
@@ -634,6 +662,7 @@ def run_ours(args, dist_):
             "late_chunks_tflops": round(late_tf, 1),
             "late_chunks_frac_peak": round(late_tf / peak_tf, 4),
             "latency_fit_vs_k": fit,
+            "schedule": schedule_summary(per_chunk_ms) if len(per_chunk_ms) > 1 else None,
             "prefill_tokens_per_s": round(w.seq_len / (attn_ms_step / 1e3), 1),
             "kv_append_bytes_per_step": int(sum(app_bytes)),
             "hbm_peak_gbs": hbm,
