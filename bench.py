@@ -267,7 +267,7 @@ def time_events(fn, iters, stream):
 class MixedSetup:
     """The mixed micro-batch resident in HBM: 4 prefill chunks + decode rows."""
 
-    def __init__(self, dev, decode_rows=None):
+    def __init__(self, dev, decode_rows=None, fp8=False):
         from chunked_prefill_causal_gb300 import vpp
         m = W.MIXED if decode_rows is None else W.MixedWorkload(n_decode=decode_rows)
         self.m = m
@@ -285,6 +285,19 @@ class MixedSetup:
                                   block_table=self.table[b].contiguous())
         self.k_new = torch.cat([ks[b][int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b]):] for b in range(B)])
         self.v_new = torch.cat([vs[b][int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b]):] for b in range(B)])
+        self.fp8 = fp8
+        if fp8:
+            # E4M3 pool with static per-kv-head scales from the value recipe
+            # (8 standard deviations map to 448, so nothing saturates).
+            s = torch.full((m.kv_heads,), 8.0 * m.std / 448.0, dtype=torch.float32, device=dev)
+            self.ks8, self.vs8 = s, s.clone()
+            self.kc8 = torch.zeros((pool, 64, m.kv_heads, m.head_dim_qk), dtype=torch.uint8, device=dev)
+            self.vc8 = torch.zeros((pool, 64, m.kv_heads, m.head_dim_v), dtype=torch.uint8, device=dev)
+            for b in range(B):
+                P = int(self.ctx[b]) - int(self.cu[b + 1] - self.cu[b])
+                if P > 0:
+                    vpp.vpp_kv_append_fp8(ks[b][:P], vs[b][:P], self.kc8, self.vc8, self.ks8, self.vs8, 0,
+                                          block_table=self.table[b].contiguous())
         del ks, vs
         self.q = q
         self.out = torch.empty((int(self.cu[-1]), m.heads, m.head_dim_v), dtype=torch.bfloat16, device=dev)
@@ -309,6 +322,22 @@ class MixedSetup:
         need_d = vpp.mixed_attn_workspace_size(self.cu_d, self.ctx_d, m.heads, m.kv_heads, m.head_dim_qk,
                                                m.head_dim_v)
         self.ws_d = torch.empty(max(need_d, 256), dtype=torch.uint8, device=dev)
+        if fp8:
+            need8 = vpp.mixed_attn_fp8_workspace_size(self.cu, self.ctx, m.heads, m.kv_heads, m.head_dim_qk,
+                                                      m.head_dim_v)
+            self.ws8 = torch.empty(max(need8, 256), dtype=torch.uint8, device=dev)
+
+    def step_fp8(self):
+        from chunked_prefill_causal_gb300 import vpp
+        vpp.vpp_kv_append_varlen_fp8(self.k_new, self.v_new, self.kc8, self.vc8, self.ks8, self.vs8, self.table,
+                                     self.cu, self.ctx)
+        vpp.vpp_mixed_attn_fp8(self.q, self.kc8, self.vc8, self.ks8, self.vs8, self.table, self.cu, self.ctx,
+                               out=self.out, lse=self.lse, workspace=self.ws8)
+
+    def decode_only_fp8(self):
+        from chunked_prefill_causal_gb300 import vpp
+        vpp.vpp_mixed_attn_fp8(self.q_d, self.kc8, self.vc8, self.ks8, self.vs8, self.table_d, self.cu_d,
+                               self.ctx_d, out=self.out_d, workspace=self.ws_d)
 
     def step(self):
         from chunked_prefill_causal_gb300 import vpp
@@ -352,6 +381,69 @@ def measure_append(dev, stream, hbm):
     byts = 2 * C * H * (dq + dv) * 2
     return {"tokens": C, "kv_heads": H, "head_dims": [dq, dv], "bytes_moved": byts, "ms": round(t, 4),
             "gbs": round(byts / (t / 1e3) / 1e9, 1), "frac_hbm": round(byts / (t / 1e3) / 1e9 / hbm, 4)}
+
+
+def measure_fp8(dev, stream, hbm, w, chunks):
+    """fp8 (E4M3) KV cache: the quantising append at the MLA-chunk size, the
+    mixed batch's decode rows and whole step over an fp8 pool, and the last
+    chunk of the chunked-prefill workload through the fp8 path (widening to
+    bf16 + the attention kernel) against the bf16 path."""
+    from chunked_prefill_causal_gb300 import vpp
+    out = {}
+    C, H, dq, dv = 24576, 128, 192, 128
+    g = torch.Generator(device=dev).manual_seed(77)
+    k = torch.randn((C, H, dq), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((C, H, dv), generator=g, device=dev).to(torch.bfloat16)
+    nb = C // 64 + 8
+    table = torch.from_numpy(W.block_table(C // 64, nb, 5)).to(dev)
+    kc = torch.empty((nb, 64, H, dq), dtype=torch.uint8, device=dev)
+    vc = torch.empty((nb, 64, H, dv), dtype=torch.uint8, device=dev)
+    s = torch.full((H,), 8.0 / 448.0, dtype=torch.float32, device=dev)
+    t = time_events(lambda: vpp.vpp_kv_append_fp8(k, v, kc, vc, s, s, 0, block_table=table), 10, stream)
+    byts = C * H * (dq + dv) * 3
+    out["append"] = {"tokens": C, "kv_heads": H, "head_dims": [dq, dv], "bytes_moved": byts, "ms": round(t, 4),
+                     "gbs": round(byts / (t / 1e3) / 1e9, 1), "frac_hbm": round(byts / (t / 1e3) / 1e9 / hbm, 4)}
+    del k, v, kc, vc
+    torch.cuda.empty_cache()
+
+    ms = MixedSetup(dev, fp8=True)
+    dec = time_events(ms.decode_only, 10, stream)
+    dec8 = time_events(ms.decode_only_fp8, 10, stream)
+    step = time_events(ms.step, 10, stream)
+    step8 = time_events(ms.step_fp8, 10, stream)
+    b8 = ms.decode_bytes // 2
+    out["decode"] = {"rows": len(ms.ctx_d), "bytes_fp8": int(b8), "ms_fp8": round(dec8, 3), "ms_bf16": round(dec, 3),
+                     "gbs_fp8": round(b8 / (dec8 / 1e3) / 1e9, 1),
+                     "frac_hbm_fp8": round(b8 / (dec8 / 1e3) / 1e9 / hbm, 4),
+                     "speedup_vs_bf16": round(dec / dec8, 3)}
+    out["mixed_step"] = {"ms_fp8": round(step8, 3), "ms_bf16": round(step, 3)}
+    del ms
+    torch.cuda.empty_cache()
+
+    # Last chunk of the chunked-prefill workload: widening + attention.
+    P, C = chunks[-1]
+    n = P + C
+    s = torch.full((w.kv_heads,), 8.0 * w.std / 448.0, dtype=torch.float32, device=dev)
+    kc8 = torch.empty((n, w.kv_heads, w.head_dim_qk), dtype=torch.uint8, device=dev)
+    vc8 = torch.empty((n, w.kv_heads, w.head_dim_v), dtype=torch.uint8, device=dev)
+    kc16 = torch.empty((n, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
+    vc16 = torch.empty((n, w.kv_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    q = None
+    for ci, (p0, c0) in enumerate(chunks):
+        qi, ki, vi = W.chunk_tensors(w, ci, dev)
+        vpp.vpp_kv_append_fp8(ki, vi, kc8, vc8, s, s, p0)
+        vpp.vpp_kv_append(ki, vi, kc16, vc16, p0)
+        q = qi
+        del ki, vi
+    o = torch.empty((C, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    ws8 = torch.empty(vpp.chunk_attn_fp8_workspace_size(P, C, w.heads, w.kv_heads, w.head_dim_qk, w.head_dim_v, 1),
+                      dtype=torch.uint8, device=dev)
+    t16 = time_events(lambda: vpp.vpp_chunk_attn_ex(q, kc16, vc16, P, out=o, num_splits=1), 5, stream)
+    t8 = time_events(lambda: vpp.vpp_chunk_attn_fp8(q, kc8, vc8, s, s, P, out=o, num_splits=1, workspace=ws8),
+                     5, stream)
+    out["prefill_last_chunk"] = {"prefix": P, "chunk": C, "ms_fp8": round(t8, 3), "ms_bf16": round(t16, 3),
+                                 "fp8_overhead": round(t8 / t16 - 1.0, 4)}
+    return out
 
 
 def measure_cost_model(dev, stream, n_batches=48, n_train=32, seed=11):
@@ -642,6 +734,8 @@ def run_ours(args, dist_):
         extras["mixed"] = measure_mixed(dev, stream, hbm, peak_tf)
         torch.cuda.empty_cache()
         extras["cost_model"] = measure_cost_model(dev, stream)
+        torch.cuda.empty_cache()
+        extras["fp8_kv"] = measure_fp8(dev, stream, hbm, w, chunks)
 
     if dist_.rank == 0:
         line = {

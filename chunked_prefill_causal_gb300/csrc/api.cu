@@ -12,6 +12,7 @@
 #include "chunk_attn.cuh"
 #include "common.cuh"
 #include "decode.cuh"
+#include "fp8.cuh"
 #include "vpp.h"
 
 namespace vpp {
@@ -178,7 +179,8 @@ size_t ws_split_bytes(int S, int64_t C, int heads, int dv) {
 int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
                     const int32_t* block_table, int32_t num_blocks, int64_t P, int64_t C,
                     int heads, int kv_heads, int dq, int dv, float scale, int num_splits,
-                    void* out, float* lse, void* workspace, size_t ws_bytes, cudaStream_t st) {
+                    void* out, float* lse, void* workspace, size_t ws_bytes, cudaStream_t st,
+                    const float* k_scale = nullptr, const float* v_scale = nullptr) {
   if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
   if (C == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
   if (!q || !k_cache || !v_cache || !out) return VPP_ERR_INVALID;
@@ -238,6 +240,8 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.lse_stride = C;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.status = ds->status;
   if (sp.n_splits > 1) {
     p.ws_o = reinterpret_cast<float*>(ws + need_q);
@@ -296,6 +300,190 @@ int build_varlen_plan(const int32_t* cu, const int32_t* ctx, int32_t batch, Varl
     plan->ctx[b] = ctx[b];
   }
   plan->cu_q[batch] = cu[batch];
+  return VPP_OK;
+}
+
+bool scales_ok(const float* k_scale, const float* v_scale) {
+  return k_scale && v_scale && !(reinterpret_cast<uintptr_t>(k_scale) & 3u) &&
+         !(reinterpret_cast<uintptr_t>(v_scale) & 3u);
+}
+
+// Sequences of a mixed batch served by the chunk-attention kernel.
+bool is_prefill_seg(const int32_t* cu, int b, int heads, int kv_heads, int dq, int dv) {
+  return cu[b + 1] > cu[b] && !is_decode_row(cu, b, heads, kv_heads, dq, dv);
+}
+
+// Bytes of the bf16 widening of the fp8 cache rows the chunk-attention
+// segments of a mixed batch read (their whole contexts).
+size_t widen_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int heads, int kv_heads,
+                      int dq, int dv) {
+  int64_t rows = 0;
+  for (int b = 0; b < batch; ++b)
+    if (is_prefill_seg(cu, b, heads, kv_heads, dq, dv)) rows += ctx[b];
+  if (rows == 0) return 0;
+  return round_up((size_t)rows * kv_heads * dq * 2, 256) + round_up((size_t)rows * kv_heads * dv * 2, 256);
+}
+
+// Mixed micro-batch over a paged cache, bf16 or (fp8) E4M3 codes with
+// per-kv-head scales.  Chunk-attention segments of an fp8 cache read the
+// bf16 widening of their contexts from the workspace; decode rows read the
+// codes directly.
+int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache,
+               const float* k_scale, const float* v_scale, const int32_t* block_table,
+               int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t* cu_seqlens_q,
+               const int32_t* ctx_lens, int32_t batch, int heads, int kv_heads, int head_dim_qk,
+               int head_dim_v, float softmax_scale, void* out, float* lse, void* workspace,
+               size_t workspace_bytes, cudaStream_t st) {
+  if (!q || !k_cache || !v_cache || !block_table || !out) return VPP_ERR_INVALID;
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return VPP_ERR_INVALID;
+  static VarlenPlan zero_plan;
+  VarlenPlan plan = zero_plan;
+  if (int r = build_varlen_plan(cu_seqlens_q, ctx_lens, batch, &plan)) return r;
+  for (int b = 0; b < batch; ++b)
+    if (ceil_div(ctx_lens[b], kBlockTokens) > max_blocks_per_seq) return VPP_ERR_INVALID;
+  const int64_t total_q = cu_seqlens_q[batch];
+  if (total_q == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+
+  // Decode rows go to the split-KV decode kernel when it supports the shape;
+  // every other sequence with queries becomes one chunk-attention segment.
+  const size_t dws = decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
+                                     head_dim_v);
+  const size_t wws =
+      fp8 ? widen_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v) : 0;
+  if (dws + wws > 0 && (!workspace || workspace_bytes < dws + wws || !aligned16(workspace)))
+    return VPP_ERR_WORKSPACE;
+
+  // Segments are ordered by per-CTA work (keys per CTA) so the heaviest CTAs
+  // start first.
+  int order[kMaxBatch];
+  int n = 0;
+  for (int b = 0; b < batch; ++b)
+    if (is_prefill_seg(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v)) order[n++] = b;
+  std::stable_sort(order, order + n, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (make_q_map(&tm_q, q, total_q, heads, kv_heads, head_dim_qk)) return VPP_ERR_INVALID;
+  int64_t kv_base[kMaxBatch];
+  if (fp8 && n > 0) {
+    static WidenPlan zero_wplan;
+    WidenPlan wp = zero_wplan;
+    wp.n = n;
+    wp.max_blocks_per_seq = max_blocks_per_seq;
+    int64_t rows = 0;
+    for (int i = 0; i < n; ++i) {
+      wp.table_row[i] = order[i];
+      wp.base[i] = rows;
+      kv_base[i] = rows;
+      rows += ctx_lens[order[i]];
+    }
+    wp.base[n] = rows;
+    if (rows > INT32_MAX / 2) return VPP_ERR_INVALID;
+    uint8_t* ws = static_cast<uint8_t*>(workspace) + dws;
+    uint16_t* k16 = reinterpret_cast<uint16_t*>(ws);
+    uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + round_up((size_t)rows * kv_heads * head_dim_qk * 2, 256));
+    if (make_contig_map(&tm_k, k16, rows, kv_heads, head_dim_qk) ||
+        make_contig_map(&tm_v, v16, rows, kv_heads, head_dim_v))
+      return VPP_ERR_INVALID;
+    if (launch_kv_widen_fp8(k_cache, v_cache, k16, v16, kv_heads, head_dim_qk, head_dim_v, block_table,
+                            num_blocks, wp, ds->status, ds->num_sms, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+  } else if (make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
+             make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v)) {
+    return VPP_ERR_INVALID;
+  }
+
+  static AttnParams zero_params;
+  AttnParams p = zero_params;
+  p.heads = heads;
+  p.kv_heads = kv_heads;
+  p.group = heads / kv_heads;
+  p.num_blocks = num_blocks;
+  p.paged = fp8 ? 0 : 1;
+  p.scale_log2 =
+      (softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)head_dim_qk)) * 1.4426950408889634f;
+  p.block_table = block_table;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.lse_stride = total_q;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
+  p.status = ds->status;
+  for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
+    const int cnt = std::min(kMaxAttnSegs, n - i0);
+    int64_t cta = 0;
+    p.n_segs = cnt;
+    for (int i = 0; i < cnt; ++i) {
+      const int b = order[i0 + i];
+      AttnSeg& s = p.segs[i];
+      s.q_start = cu_seqlens_q[b];
+      s.q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+      s.kv_len = ctx_lens[b];
+      s.table_off = b * max_blocks_per_seq;
+      s.n_pairs = pairs_for(s.q_len, p.group);
+      s.n_splits = 1;
+      s.split_keys = 0;
+      s.cta_begin = (int32_t)cta;
+      s.kv_base = fp8 ? (int32_t)kv_base[i0 + i] : 0;
+      s.ws_row0 = 0;
+      cta += (int64_t)s.n_pairs * kv_heads;
+    }
+    if (cta > INT32_MAX) return VPP_ERR_INVALID;
+    if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+  }
+
+  // Decode rows, longest context first.
+  static DecodeParams zero_dp;
+  DecodeParams dp = zero_dp;
+  int drows[kMaxBatch];
+  int nd = 0;
+  for (int b = 0; b < batch; ++b)
+    if (is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v) && ctx_lens[b] > 0)
+      drows[nd++] = b;
+  if (nd > 0) {
+    std::stable_sort(drows, drows + nd, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
+    int64_t items = 0;
+    for (int i = 0; i < nd; ++i) {
+      const int b = drows[i];
+      dp.rows[i].b = b;
+      dp.rows[i].q_row = cu_seqlens_q[b];
+      dp.rows[i].ctx = ctx_lens[b];
+      dp.rows[i].item0 = (int32_t)items;
+      items += ceil_div(ctx_lens[b], kDecodeSplitTokens);
+    }
+    if (items > INT32_MAX) return VPP_ERR_INVALID;
+    dp.n_rows = nd;
+    dp.heads = heads;
+    dp.kv_heads = kv_heads;
+    dp.split_tokens = kDecodeSplitTokens;
+    dp.num_blocks = num_blocks;
+    dp.max_blocks_per_seq = max_blocks_per_seq;
+    dp.scale_log2 = p.scale_log2;
+    dp.q = static_cast<const uint16_t*>(q);
+    dp.k_cache = k_cache;
+    dp.v_cache = v_cache;
+    dp.k_scale = fp8 ? k_scale : nullptr;
+    dp.v_scale = fp8 ? v_scale : nullptr;
+    dp.block_table = block_table;
+    dp.out = static_cast<uint16_t*>(out);
+    dp.lse = lse;
+    dp.lse_stride = total_q;
+    if (dws > 0) {
+      dp.ws_o = static_cast<float*>(workspace);
+      dp.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           round_up((size_t)items * heads * head_dim_v * 4, 256));
+    }
+    dp.status = ds->status;
+    if (launch_decode(dp, (int)items, head_dim_qk, fp8, ds->num_sms, st) != cudaSuccess)
+      return VPP_ERR_CUDA;
+  }
   return VPP_OK;
 }
 
@@ -432,128 +620,9 @@ int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,
                    int heads, int kv_heads, int head_dim_qk, int head_dim_v,
                    float softmax_scale, void* out, float* lse, void* workspace,
                    size_t workspace_bytes, void* stream) {
-  if (!q || !k_cache || !v_cache || !block_table || !out) return VPP_ERR_INVALID;
-  if (num_blocks <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
-  if (int r = check_heads(heads, kv_heads)) return r;
-  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return VPP_ERR_INVALID;
-  static VarlenPlan zero_plan;
-  VarlenPlan plan = zero_plan;
-  if (int r = build_varlen_plan(cu_seqlens_q, ctx_lens, batch, &plan)) return r;
-  for (int b = 0; b < batch; ++b)
-    if (ceil_div(ctx_lens[b], kBlockTokens) > max_blocks_per_seq) return VPP_ERR_INVALID;
-  const int64_t total_q = cu_seqlens_q[batch];
-  if (total_q == 0) return VPP_OK;
-  DeviceState* ds = nullptr;
-  if (int r = device_state(&ds)) return r;
-  cudaStream_t st = as_stream(stream);
-
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (make_q_map(&tm_q, q, total_q, heads, kv_heads, head_dim_qk) ||
-      make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
-      make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v))
-    return VPP_ERR_INVALID;
-
-  static AttnParams zero_params;
-  AttnParams p = zero_params;
-  p.heads = heads;
-  p.kv_heads = kv_heads;
-  p.group = heads / kv_heads;
-  p.num_blocks = num_blocks;
-  p.paged = 1;
-  p.scale_log2 =
-      (softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)head_dim_qk)) * 1.4426950408889634f;
-  p.block_table = block_table;
-  p.out = static_cast<uint16_t*>(out);
-  p.lse = lse;
-  p.lse_stride = total_q;
-  p.status = ds->status;
-
-  // Decode rows go to the split-KV decode kernel when it supports the shape;
-  // every other sequence with queries becomes one chunk-attention segment.
-  const size_t dws = decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
-                                     head_dim_v);
-  if (dws > 0 && (!workspace || workspace_bytes < dws || !aligned16(workspace)))
-    return VPP_ERR_WORKSPACE;
-
-  // Every sequence with queries becomes one segment; segments are ordered by
-  // per-CTA work (keys per CTA) so the heaviest CTAs start first.
-  int order[kMaxBatch];
-  int n = 0;
-  for (int b = 0; b < batch; ++b)
-    if (cu_seqlens_q[b + 1] > cu_seqlens_q[b] &&
-        !is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v))
-      order[n++] = b;
-  std::stable_sort(order, order + n, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
-  for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
-    const int cnt = std::min(kMaxAttnSegs, n - i0);
-    int64_t cta = 0;
-    p.n_segs = cnt;
-    for (int i = 0; i < cnt; ++i) {
-      const int b = order[i0 + i];
-      AttnSeg& s = p.segs[i];
-      s.q_start = cu_seqlens_q[b];
-      s.q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-      s.kv_len = ctx_lens[b];
-      s.table_off = b * max_blocks_per_seq;
-      s.n_pairs = pairs_for(s.q_len, p.group);
-      s.n_splits = 1;
-      s.split_keys = 0;
-      s.cta_begin = (int32_t)cta;
-      s.ws_row0 = 0;
-      cta += (int64_t)s.n_pairs * kv_heads;
-    }
-    if (cta > INT32_MAX) return VPP_ERR_INVALID;
-    if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) !=
-        cudaSuccess)
-      return VPP_ERR_CUDA;
-  }
-
-  // Decode rows, longest context first.
-  static DecodeParams zero_dp;
-  DecodeParams dp = zero_dp;
-  int drows[kMaxBatch];
-  int nd = 0;
-  for (int b = 0; b < batch; ++b)
-    if (is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v) && ctx_lens[b] > 0)
-      drows[nd++] = b;
-  if (nd > 0) {
-    std::stable_sort(drows, drows + nd, [&](int a, int b) { return ctx_lens[a] > ctx_lens[b]; });
-    int64_t items = 0;
-    for (int i = 0; i < nd; ++i) {
-      const int b = drows[i];
-      dp.rows[i].b = b;
-      dp.rows[i].q_row = cu_seqlens_q[b];
-      dp.rows[i].ctx = ctx_lens[b];
-      dp.rows[i].item0 = (int32_t)items;
-      items += ceil_div(ctx_lens[b], kDecodeSplitTokens);
-    }
-    if (items > INT32_MAX) return VPP_ERR_INVALID;
-    dp.n_rows = nd;
-    dp.heads = heads;
-    dp.kv_heads = kv_heads;
-    dp.split_tokens = kDecodeSplitTokens;
-    dp.num_blocks = num_blocks;
-    dp.max_blocks_per_seq = max_blocks_per_seq;
-    dp.scale_log2 = p.scale_log2;
-    dp.q = static_cast<const uint16_t*>(q);
-    dp.k_cache = static_cast<const uint16_t*>(k_cache);
-    dp.v_cache = static_cast<const uint16_t*>(v_cache);
-    dp.block_table = block_table;
-    dp.out = static_cast<uint16_t*>(out);
-    dp.lse = lse;
-    dp.lse_stride = total_q;
-    if (dws > 0) {
-      dp.ws_o = static_cast<float*>(workspace);
-      dp.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                           round_up((size_t)items * heads * head_dim_v * 4, 256));
-    }
-    dp.status = ds->status;
-    if (launch_decode(dp, (int)items, head_dim_qk, ds->num_sms, st) != cudaSuccess)
-      return VPP_ERR_CUDA;
-  }
-  return VPP_OK;
+  return mixed_impl(false, q, k_cache, v_cache, nullptr, nullptr, block_table, max_blocks_per_seq,
+                    num_blocks, cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
+                    head_dim_v, softmax_scale, out, lse, workspace, workspace_bytes, as_stream(stream));
 }
 
 size_t vpp_mixed_attn_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
@@ -562,6 +631,130 @@ size_t vpp_mixed_attn_workspace_size(const int32_t* cu_seqlens_q, const int32_t*
   if (!cu_seqlens_q || !ctx_lens || batch <= 0 || batch > kMaxBatch) return 0;
   if (check_heads(heads, kv_heads) != VPP_OK) return 0;
   return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v);
+}
+
+// ------------------------------------------------------------- fp8 (E4M3) KV cache
+int vpp_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const float* k_scale, const float* v_scale, const int32_t* block_table,
+                      int32_t num_blocks, int64_t prefix_len, int64_t chunk_len, int kv_heads,
+                      int head_dim_qk, int head_dim_v, void* stream) {
+  if (prefix_len < 0 || chunk_len < 0 || num_blocks <= 0 || kv_heads <= 0) return VPP_ERR_INVALID;
+  if (chunk_len == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
+  if (!k_new || !v_new || !k_cache || !v_cache || !scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
+  if (head_dim_qk <= 0 || head_dim_v <= 0 || head_dim_qk % 64 || head_dim_v % 64)
+    return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return VPP_ERR_INVALID;
+  const int64_t end = prefix_len + chunk_len;
+  if (block_table ? (int64_t)num_blocks * kBlockTokens < end : (int64_t)num_blocks < end)
+    return VPP_ERR_INVALID;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  if (launch_kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, num_blocks,
+                           prefix_len, chunk_len, kv_heads, head_dim_qk, head_dim_v, ds->status,
+                           ds->num_sms, as_stream(stream)) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return VPP_OK;
+}
+
+int vpp_kv_append_varlen_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const float* k_scale, const float* v_scale, const int32_t* block_table,
+                             int32_t max_blocks_per_seq, int32_t num_blocks,
+                             const int32_t* cu_seqlens_q, const int32_t* ctx_lens, int32_t batch,
+                             int kv_heads, int head_dim_qk, int head_dim_v, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !scales_ok(k_scale, v_scale))
+    return VPP_ERR_INVALID;
+  if (num_blocks <= 0 || kv_heads <= 0 || max_blocks_per_seq <= 0) return VPP_ERR_INVALID;
+  if (head_dim_qk <= 0 || head_dim_v <= 0 || head_dim_qk % 64 || head_dim_v % 64)
+    return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return VPP_ERR_INVALID;
+  static VarlenPlan zero_plan;
+  VarlenPlan plan = zero_plan;
+  plan.max_blocks_per_seq = max_blocks_per_seq;
+  if (int r = build_varlen_plan(cu_seqlens_q, ctx_lens, batch, &plan)) return r;
+  for (int b = 0; b < batch; ++b)
+    if (ceil_div(ctx_lens[b], kBlockTokens) > max_blocks_per_seq) return VPP_ERR_INVALID;
+  if (plan.cu_q[batch] == 0) return VPP_OK;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  if (launch_kv_append_fp8_varlen(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, plan,
+                                  num_blocks, kv_heads, head_dim_qk, head_dim_v, ds->status, ds->num_sms,
+                                  as_stream(stream)) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return VPP_OK;
+}
+
+int vpp_chunk_attn_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, const int32_t* block_table, int32_t num_blocks,
+                       int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads, int head_dim_qk,
+                       int head_dim_v, float softmax_scale, int num_splits, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const int64_t P = prefix_len, C = chunk_len;
+  if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
+  if (C == 0) return VPP_OK;
+  if (!q || !k_cache || !v_cache || !out || !scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return VPP_ERR_INVALID;
+  if (P + C > (int64_t)INT32_MAX / 2) return VPP_ERR_INVALID;
+  if (block_table ? (int64_t)num_blocks * kBlockTokens < P + C : (int64_t)num_blocks < P + C)
+    return VPP_ERR_INVALID;
+  const int64_t n = P + C;
+  const size_t kb = round_up((size_t)n * kv_heads * head_dim_qk * 2, 256);
+  const size_t wb = kb + round_up((size_t)n * kv_heads * head_dim_v * 2, 256);
+  const size_t rest = vpp_chunk_attn_workspace_size(VPP_BF16, P, C, heads, kv_heads, head_dim_qk,
+                                                    head_dim_v, num_splits);
+  if (!workspace || workspace_bytes < wb + rest || !aligned16(workspace)) return VPP_ERR_WORKSPACE;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  cudaStream_t st = as_stream(stream);
+  static WidenPlan zero_plan;
+  WidenPlan wp = zero_plan;
+  wp.n = 1;
+  wp.base[1] = n;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + kb);
+  if (launch_kv_widen_fp8(k_cache, v_cache, k16, v16, kv_heads, head_dim_qk, head_dim_v, block_table,
+                          num_blocks, wp, ds->status, ds->num_sms, st) != cudaSuccess)
+    return VPP_ERR_CUDA;
+  return chunk_attn_impl(q, VPP_BF16, k16, v16, nullptr, (int32_t)n, P, C, heads, kv_heads, head_dim_qk,
+                         head_dim_v, softmax_scale, num_splits, out, lse, ws + wb, workspace_bytes - wb,
+                         st, k_scale, v_scale);
+}
+
+size_t vpp_chunk_attn_fp8_workspace_size(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
+                                         int head_dim_qk, int head_dim_v, int num_splits) {
+  if (prefix_len < 0 || chunk_len <= 0 || kv_heads <= 0 || head_dim_qk <= 0 || head_dim_v <= 0) return 0;
+  const int64_t n = prefix_len + chunk_len;
+  return round_up((size_t)n * kv_heads * head_dim_qk * 2, 256) +
+         round_up((size_t)n * kv_heads * head_dim_v * 2, 256) +
+         vpp_chunk_attn_workspace_size(VPP_BF16, prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
+                                       head_dim_v, num_splits);
+}
+
+int vpp_mixed_attn_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, const int32_t* block_table, int32_t max_blocks_per_seq,
+                       int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                       int32_t batch, int heads, int kv_heads, int head_dim_qk, int head_dim_v,
+                       float softmax_scale, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
+  return mixed_impl(true, q, k_cache, v_cache, k_scale, v_scale, block_table, max_blocks_per_seq,
+                    num_blocks, cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
+                    head_dim_v, softmax_scale, out, lse, workspace, workspace_bytes, as_stream(stream));
+}
+
+size_t vpp_mixed_attn_fp8_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                         int32_t batch, int heads, int kv_heads, int head_dim_qk,
+                                         int head_dim_v) {
+  if (!cu_seqlens_q || !ctx_lens || batch <= 0 || batch > kMaxBatch) return 0;
+  if (check_heads(heads, kv_heads) != VPP_OK) return 0;
+  return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v) +
+         widen_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v);
 }
 
 int vpp_last_device_status(void* stream, int* code) {

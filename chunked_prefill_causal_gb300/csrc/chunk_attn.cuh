@@ -23,6 +23,8 @@ struct AttnSeg {
   int32_t n_splits;    // key ranges (1 = write the final output directly)
   int32_t split_keys;  // keys per non-final range, multiple of kTileN
   int32_t cta_begin;   // first CTA index of this segment
+  int32_t kv_base;     // contiguous cache: row of the segment's key 0
+  int32_t pad0;
   int64_t ws_row0;     // first workspace row of this segment's partials
 };
 
@@ -41,6 +43,8 @@ struct AttnParams {
   int64_t lse_stride;
   float* ws_o;            // split partials, float32 [rows][heads][dv]
   float* ws_lse;          // [rows][heads]
+  const float* k_scale;   // [kv_heads] factor on every key (fp8 cache), may be null
+  const float* v_scale;   // [kv_heads] factor on every value (fp8 cache), may be null
   int* status;
   AttnSeg segs[kMaxAttnSegs];
 };

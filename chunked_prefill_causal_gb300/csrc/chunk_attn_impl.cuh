@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c0 = block_coord(key0 / kBlockTokens);
           c1 = block_coord(key0 / kBlockTokens + 1);
         } else {
-          c0 = key0;
-          c1 = key0 + kBlockTokens;
+          c0 = seg.kv_base + key0;
+          c1 = c0 + kBlockTokens;
         }
         for (int part = 0; part < 2; ++part) {  // K, then V
           const int t = 2 * j + part;
@@ -385,7 +385,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + x * kTileN;
     const uint32_t tO = lane_base + 2 * kTileN + x * DV;
-    const float sl = p.scale_log2;
+    // Per-kv-head factors of an fp8 cache (key codes x k_scale, values x
+    // v_scale): k_scale joins the score scale, v_scale the final division.
+    const float sl = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
+    const float vsc = p.v_scale ? __ldg(p.v_scale + g) : 1.f;
     float m = -INFINITY;  // running max of score * scale * log2(e)
     float l = 0.f;        // running denominator, relative to 2^m
     bool ok = true;
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok) {
       tc_fence_after();
       const bool valid = tok < seg.q_len;
-      const float inv = 1.f / l;
+      const float inv = vsc / l;
       const float lse_v = m * kLn2 + logf(l);
       if (seg.n_splits == 1) {
         uint16_t* orow = p.out + (static_cast<int64_t>(seg.q_start + tok) * p.heads + hq) * DV;

@@ -25,6 +25,10 @@
 // partial output and its LSE go to the workspace and decode_merge combines
 // them ("02 · 并行策略与 PP 切分" note, §7).  HBM-bound: the algorithmic bytes
 // are ctx x Hkv x (dq + dv) x 2 per row plus q, out and the partials.
+//
+// fp8 cache (F8): the stages hold E4M3 codes, widened exactly to float in
+// registers; kv head h's k_scale joins its score scale and its v_scale
+// multiplies the output, so the cache bytes per row halve.
 #include <algorithm>
 
 #include "common.cuh"
@@ -50,13 +54,24 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-template <int D, int G>
+// 8 E4M3 codes -> 8 floats (exact).
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float* f) {
+  const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w.x & 0xFFFFu));
+  const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w.x >> 16));
+  const float2 c = e4m3x2_to_f32x2(static_cast<uint16_t>(w.y & 0xFFFFu));
+  const float2 d = e4m3x2_to_f32x2(static_cast<uint16_t>(w.y >> 16));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int DPL = D / 8;     // score dims per lane (8 lanes per token)
   constexpr int OPL = D / 32;    // output dims per lane
+  constexpr int ESZ = F8 ? 1 : 2;  // cache bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = p.kv_heads;
-  const int row_bytes = hkv * D * 2;                 // one token, all kv heads
+  const int row_bytes = hkv * D * ESZ;               // one token, all kv heads
   const int stage_bytes = 2 * kStepTokens * row_bytes;  // K then V
   const int nstage = min(8, 196608 / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + 196608);  // [hkv][16][G]
@@ -111,11 +126,11 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         const uint32_t full = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * stage_bytes);
         if (blk >= 0) {
-          const int64_t off = (static_cast<int64_t>(blk) * kBlockTokens + t0 % kBlockTokens) * hkv * D;
+          const int64_t off = (static_cast<int64_t>(blk) * kBlockTokens + t0 % kBlockTokens) * row_bytes;
           const uint32_t bytes = static_cast<uint32_t>(nt * row_bytes);
           mbar_arrive_expect_tx(full, 2 * bytes);
-          bulk_g2s(dst, p.k_cache + off, bytes, full);
-          bulk_g2s(dst + kStepTokens * row_bytes, p.v_cache + off, bytes, full);
+          bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
+          bulk_g2s(dst + kStepTokens * row_bytes, static_cast<const uint8_t*>(p.v_cache) + off, bytes, full);
         } else {
           mbar_arrive(full);  // invalid block: the step's rows are skipped
         }
@@ -150,7 +165,8 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         bf16x2_to_f32(w.w, qf[j][8 * c + 6], qf[j][8 * c + 7]);
       }
     }
-    const float sl = p.scale_log2;
+    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
+    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
     float m[G], lpart[G], o[G][OPL];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
@@ -180,15 +196,19 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < G; ++j) acc[j] = 0.f;
         if (t < nt) {
-          const uint4* kr = reinterpret_cast<const uint4*>(kst + t * row_bytes + h * D * 2 + r * DPL * 2);
+          const uint8_t* kb = kst + t * row_bytes + (h * D + r * DPL) * ESZ;
 #pragma unroll
           for (int c = 0; c < DPL / 8; ++c) {
-            const uint4 w = kr[c];
             float kf[8];
-            bf16x2_to_f32(w.x, kf[0], kf[1]);
-            bf16x2_to_f32(w.y, kf[2], kf[3]);
-            bf16x2_to_f32(w.z, kf[4], kf[5]);
-            bf16x2_to_f32(w.w, kf[6], kf[7]);
+            if (F8) {
+              e4m3x8_to_f32(reinterpret_cast<const uint2*>(kb)[c], kf);
+            } else {
+              const uint4 w = reinterpret_cast<const uint4*>(kb)[c];
+              bf16x2_to_f32(w.x, kf[0], kf[1]);
+              bf16x2_to_f32(w.y, kf[2], kf[3]);
+              bf16x2_to_f32(w.z, kf[4], kf[5]);
+              bf16x2_to_f32(w.w, kf[6], kf[7]);
+            }
 #pragma unroll
             for (int j = 0; j < G; ++j)
 #pragma unroll
@@ -232,9 +252,24 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float pv[G];
 #pragma unroll
         for (int j = 0; j < G; ++j) pv[j] = pw[t * G + j];
-        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vst + t * row_bytes + h * D * 2) + lane * OPL;
+        const uint8_t* vb = vst + t * row_bytes + (h * D + lane * OPL) * ESZ;
+        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vb);
         float vf[OPL];
-        if (OPL == 4) {
+        if (F8) {
+          if (OPL == 4) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vb);
+            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w & 0xFFFFu));
+            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w >> 16));
+            vf[0] = a.x;
+            vf[1 % OPL] = a.y;
+            vf[2 % OPL] = b.x;
+            vf[3 % OPL] = b.y;
+          } else {
+            const float2 a = e4m3x2_to_f32x2(*vr);
+            vf[0] = a.x;
+            vf[1 % OPL] = a.y;
+          }
+        } else if (OPL == 4) {
           const uint2 w = *reinterpret_cast<const uint2*>(vr);
           bf16x2_to_f32(w.x, vf[0], vf[1 % OPL]);
           bf16x2_to_f32(w.y, vf[2 % OPL], vf[3 % OPL]);
@@ -260,7 +295,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float l = lpart[j];
 #pragma unroll
         for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
-        const float inv = 1.f / l;
+        const float inv = vsc / l;
         const float lse_v = m[j] * kLn2d + logf(l);
         const int hq = h * G + j;
         if (n_splits == 1) {
@@ -325,18 +360,19 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t st) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    e = cudaFuncSetAttribute(decode_kernel<D, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kDecodeSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  decode_kernel<D, G><<<items, 32 * (p.kv_heads + 1), kDecodeSmem, st>>>(p);
+  decode_kernel<D, G, F8><<<items, 32 * (p.kv_heads + 1), kDecodeSmem, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int grid = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(p.n_rows) * p.heads + 7) / 8,
@@ -356,20 +392,26 @@ bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads) 
   return g == 1 || g == 2 || g == 4 || (g == 8 && head_dim_qk == 64);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, int num_sms,
-                          cudaStream_t stream) {
+template <bool F8>
+cudaError_t launch_f(const DecodeParams& p, int items, int head_dim, int num_sms, cudaStream_t stream) {
   const int g = p.heads / p.kv_heads;
   if (head_dim == 128) {
-    if (g == 1) return launch_t<128, 1>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<128, 2>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<128, 4>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<128, 1, F8>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<128, 2, F8>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<128, 4, F8>(p, items, num_sms, stream);
   } else if (head_dim == 64) {
-    if (g == 1) return launch_t<64, 1>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<64, 2>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<64, 4>(p, items, num_sms, stream);
-    if (g == 8) return launch_t<64, 8>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<64, 1, F8>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<64, 2, F8>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<64, 4, F8>(p, items, num_sms, stream);
+    if (g == 8) return launch_t<64, 8, F8>(p, items, num_sms, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, int num_sms,
+                          cudaStream_t stream) {
+  return fp8 ? launch_f<true>(p, items, head_dim, num_sms, stream)
+             : launch_f<false>(p, items, head_dim, num_sms, stream);
 }
 
 }  // namespace vpp

@@ -26,8 +26,10 @@ struct DecodeParams {
   float scale_log2;
   int32_t pad0;
   const uint16_t* q;           // bf16 [total_q][heads][d]
-  const uint16_t* k_cache;     // bf16 [num_blocks][64][kv_heads][d]
-  const uint16_t* v_cache;
+  const void* k_cache;         // [num_blocks][64][kv_heads][d], bf16 or E4M3 codes
+  const void* v_cache;
+  const float* k_scale;        // E4M3 cache: [kv_heads] factors (null for bf16)
+  const float* v_scale;
   const int32_t* block_table;  // [batch][max_blocks_per_seq]
   uint16_t* out;               // bf16 [total_q][heads][d]
   float* lse;                  // [heads][lse_stride], may be null
@@ -45,7 +47,8 @@ constexpr int kDecodeSplitTokens = 1024;
 // kv_heads <= 8, heads / kv_heads in {1, 2, 4}, or 8 when dq = 64).
 bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads);
 
-cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, int num_sms,
+// fp8: the cache holds E4M3 codes with per-kv-head k_scale / v_scale.
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, int num_sms,
                           cudaStream_t stream);
 
 }  // namespace vpp

@@ -308,4 +308,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ------------------------------------------------------------------ fp8 E4M3
+// Two E4M3 codes (lo = the byte at the lower address) from two floats, round
+// to nearest even, magnitudes beyond the largest finite value (448) clamped.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes to two floats (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  float2 f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(h2));
+  return f;
+}
+
 }  // namespace vpp

@@ -43,6 +43,18 @@ SIGNATURES = {
     "vpp_mixed_attn_workspace_size": ([_c_void_p, _c_void_p, _i32, _int, _int, _int, _int], _sz),
     "vpp_kv_append_varlen": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
                               _c_void_p, _c_void_p, _i32, _int, _int, _int, _c_void_p], _int),
+    "vpp_kv_append_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32,
+                           _i64, _i64, _int, _int, _int, _c_void_p], _int),
+    "vpp_kv_append_varlen_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                  _i32, _i32, _c_void_p, _c_void_p, _i32, _int, _int, _int, _c_void_p], _int),
+    "vpp_chunk_attn_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64, _i64,
+                            _int, _int, _int, _int, _f32, _int, _c_void_p, _c_void_p, _c_void_p, _sz,
+                            _c_void_p], _int),
+    "vpp_chunk_attn_fp8_workspace_size": ([_i64, _i64, _int, _int, _int, _int, _int], _sz),
+    "vpp_mixed_attn_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
+                            _c_void_p, _c_void_p, _i32, _int, _int, _int, _int, _f32, _c_void_p, _c_void_p,
+                            _c_void_p, _sz, _c_void_p], _int),
+    "vpp_mixed_attn_fp8_workspace_size": ([_c_void_p, _c_void_p, _i32, _int, _int, _int, _int], _sz),
     "vpp_last_device_status": ([_c_void_p, ctypes.POINTER(_int)], _int),
     "vpp_selftest_wait_timeout": ([_int, _c_void_p], _int),
 }
@@ -238,6 +250,109 @@ def vpp_mixed_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, ctx_lens, out
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         k_cache.shape[0], cu_p, ctx_p, len(ctx), H, Hkv, dq, dv, float(softmax_scale), _ptr(out),
         _ptr(lse), _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- fp8 (E4M3) KV cache
+def _fp8_cache(*caches):
+    for c in caches:
+        if c.dtype != torch.uint8:
+            raise ValueError("fp8 caches hold E4M3 codes as uint8")
+
+
+def _scales(k_scale, v_scale, kv_heads):
+    _need_cuda(k_scale, v_scale)
+    for s in (k_scale, v_scale):
+        if s.dtype != torch.float32 or s.numel() != kv_heads:
+            raise ValueError("scales are float32 CUDA tensors with one entry per kv head")
+
+
+def vpp_kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, prefix_len, block_table=None,
+                      stream=None):
+    """Quantise a chunk's bf16 K/V ([C, Hkv, d]) into an E4M3 cache (uint8),
+    one float32 scale per kv head (code = E4M3(fl32(x / scale)))."""
+    _need_cuda(k_new, v_new, k_cache, v_cache, block_table)
+    _fp8_cache(k_cache, v_cache)
+    if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16:
+        raise ValueError("fp8 append takes bf16 K/V")
+    C, Hkv, dq = k_new.shape
+    dv = v_new.shape[2]
+    _scales(k_scale, v_scale, Hkv)
+    _check("vpp_kv_append_fp8", load().vpp_kv_append_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), k_cache.shape[0], int(prefix_len), C, Hkv, dq, dv, _stream(stream)))
+
+
+def vpp_kv_append_varlen_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q,
+                             ctx_lens, stream=None):
+    """Varlen append into an E4M3 paged cache (see vpp_kv_append_varlen)."""
+    _need_cuda(k_new, v_new, k_cache, v_cache, block_table)
+    _fp8_cache(k_cache, v_cache)
+    _, Hkv, dq = k_new.shape
+    dv = v_new.shape[2]
+    _scales(k_scale, v_scale, Hkv)
+    cu, cu_p = _i32_host(cu_seqlens_q)
+    ctx, ctx_p = _i32_host(ctx_lens)
+    _check("vpp_kv_append_varlen_fp8", load().vpp_kv_append_varlen_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), block_table.shape[1], k_cache.shape[0], cu_p, ctx_p, len(ctx), Hkv, dq, dv,
+        _stream(stream)))
+
+
+def chunk_attn_fp8_workspace_size(prefix_len, chunk_len, heads, kv_heads, dq, dv, num_splits=0):
+    return int(load().vpp_chunk_attn_fp8_workspace_size(int(prefix_len), int(chunk_len), heads, kv_heads,
+                                                        dq, dv, num_splits))
+
+
+def vpp_chunk_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, prefix_len, block_table=None, out=None,
+                       lse=None, softmax_scale=0.0, num_splits=0, workspace=None, stream=None):
+    """Chunk attention over an E4M3 cache (bf16 q), paged or contiguous."""
+    _need_cuda(q, k_cache, v_cache, block_table, out, lse, workspace)
+    _fp8_cache(k_cache, v_cache)
+    C, H, dq = q.shape
+    Hkv = k_cache.shape[-2]
+    dv = v_cache.shape[-1]
+    _scales(k_scale, v_scale, Hkv)
+    if out is None:
+        out = torch.empty((C, H, dv), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        need = chunk_attn_fp8_workspace_size(prefix_len, C, H, Hkv, dq, dv, num_splits)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check("vpp_chunk_attn_fp8", load().vpp_chunk_attn_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        k_cache.shape[0], int(prefix_len), C, H, Hkv, dq, dv, float(softmax_scale), int(num_splits),
+        _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+def mixed_attn_fp8_workspace_size(cu_seqlens_q, ctx_lens, heads, kv_heads, dq, dv):
+    cu, cu_p = _i32_host(cu_seqlens_q)
+    ctx, ctx_p = _i32_host(ctx_lens)
+    return int(load().vpp_mixed_attn_fp8_workspace_size(cu_p, ctx_p, len(ctx), heads, kv_heads, dq, dv))
+
+
+def vpp_mixed_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, ctx_lens, out=None,
+                       lse=None, softmax_scale=0.0, workspace=None, stream=None):
+    """Mixed micro-batch over an E4M3 paged cache (host cu_seqlens_q / ctx_lens)."""
+    _need_cuda(q, k_cache, v_cache, block_table, out, lse, workspace)
+    _fp8_cache(k_cache, v_cache)
+    T, H, dq = q.shape
+    Hkv = k_cache.shape[2]
+    dv = v_cache.shape[3]
+    _scales(k_scale, v_scale, Hkv)
+    cu, cu_p = _i32_host(cu_seqlens_q)
+    ctx, ctx_p = _i32_host(ctx_lens)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
+    need = mixed_attn_fp8_workspace_size(cu, ctx, H, Hkv, dq, dv)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("vpp_mixed_attn_fp8", load().vpp_mixed_attn_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], k_cache.shape[0], cu_p, ctx_p, len(ctx), H, Hkv, dq, dv, float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream)))
     return out
 
 

@@ -230,6 +230,95 @@ int vpp_kv_append_varlen(const void *k_new, const void *v_new, void *k_cache,
                          int head_dim_v, void *stream);
 
 /*
+ * fp8 KV cache ([GLM PP note] §1, §3.2: the deployment keeps its KV cache in
+ * fp8, about half the bytes per token of bf16, which nearly doubles the
+ * tokens one GPU holds).
+ *
+ * Element format: E4M3 of the OCP 8-bit floating point specification (1 sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits, largest finite value
+ * 448, no infinities), one uint8 code per element, in the same layouts as the
+ * bf16 cache (paged [num_blocks][64][kv_heads][d], or contiguous
+ * [capacity][kv_heads][d] when block_table == NULL).
+ * Scaling: k_scale and v_scale are DEVICE float32 [kv_heads], 4-byte aligned,
+ * one factor per kv head, finite and > 0 (not checked on the device); an
+ * element's value is E4M3(code) x scale.  The pages give only the byte
+ * counts; the per-kv-head scaling is this library's reading.
+ * NULL scales return VPP_ERR_INVALID.
+ */
+
+/*
+ * a1 over an fp8 cache.  k_new/v_new are bf16 [chunk_len][kv_heads][d]; each
+ * value x becomes code = E4M3(fl32(x / scale)): the float32 quotient (IEEE
+ * round to nearest even) rounded to the nearest E4M3 value, ties to the even
+ * code, magnitudes above 448 clamped to 448, the sign of zero kept.
+ * Everything else as vpp_kv_append.
+ */
+int vpp_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache,
+                      void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_table,
+                      int32_t num_blocks, int64_t prefix_len,
+                      int64_t chunk_len, int kv_heads, int head_dim_qk,
+                      int head_dim_v, void *stream);
+
+/* Varlen append (as vpp_kv_append_varlen) into an fp8 cache. */
+int vpp_kv_append_varlen_fp8(const void *k_new, const void *v_new,
+                             void *k_cache, void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_table,
+                             int32_t max_blocks_per_seq, int32_t num_blocks,
+                             const int32_t *cu_seqlens_q,
+                             const int32_t *ctx_lens, int32_t batch,
+                             int kv_heads, int head_dim_qk, int head_dim_v,
+                             void *stream);
+
+/*
+ * a2..a7 over an fp8 cache: the contract of vpp_chunk_attn_ex with a bf16 q
+ * and K, V read as code x scale.  The keys 0 .. prefix_len + chunk_len - 1
+ * are first widened to bf16 in the workspace (exact: every E4M3 value is a
+ * bf16 value); the attention kernel then multiplies scores by k_scale and the
+ * output by v_scale of the row's kv head.  workspace: DEVICE, at least
+ * vpp_chunk_attn_fp8_workspace_size(...) bytes, never NULL for chunk_len > 0.
+ */
+int vpp_chunk_attn_fp8(const void *q, const void *k_cache,
+                       const void *v_cache, const float *k_scale,
+                       const float *v_scale, const int32_t *block_table,
+                       int32_t num_blocks, int64_t prefix_len,
+                       int64_t chunk_len, int heads, int kv_heads,
+                       int head_dim_qk, int head_dim_v, float softmax_scale,
+                       int num_splits, void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/* Workspace bytes vpp_chunk_attn_fp8 needs for these arguments. */
+size_t vpp_chunk_attn_fp8_workspace_size(int64_t prefix_len,
+                                         int64_t chunk_len, int heads,
+                                         int kv_heads, int head_dim_qk,
+                                         int head_dim_v, int num_splits);
+
+/*
+ * a8..a9 over an fp8 paged cache: the contract of vpp_mixed_attn.  Decode
+ * rows read the codes directly (the decode kernel's shapes as in
+ * vpp_mixed_attn); every other sequence with queries reads the bf16 widening
+ * of its whole context from the workspace.  workspace >=
+ * vpp_mixed_attn_fp8_workspace_size(...) bytes.
+ */
+int vpp_mixed_attn_fp8(const void *q, const void *k_cache,
+                       const void *v_cache, const float *k_scale,
+                       const float *v_scale, const int32_t *block_table,
+                       int32_t max_blocks_per_seq, int32_t num_blocks,
+                       const int32_t *cu_seqlens_q, const int32_t *ctx_lens,
+                       int32_t batch, int heads, int kv_heads,
+                       int head_dim_qk, int head_dim_v, float softmax_scale,
+                       void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/* Workspace bytes vpp_mixed_attn_fp8 needs (HOST cu_seqlens_q / ctx_lens). */
+size_t vpp_mixed_attn_fp8_workspace_size(const int32_t *cu_seqlens_q,
+                                         const int32_t *ctx_lens,
+                                         int32_t batch, int heads,
+                                         int kv_heads, int head_dim_qk,
+                                         int head_dim_v);
+
+/*
  * Device status word: synchronises `stream`, stores the first error any
  * kernel of this library recorded since the last reset (VPP_OK if none) in
  * *code, and resets the word to VPP_OK.  Returns VPP_ERR_CUDA if the

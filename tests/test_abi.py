@@ -71,6 +71,34 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.vpp_mixed_attn(fake, fake, fake, fake, 4, 16, cu, ctx, 2, 8, 2, 128, 128, 0.0, fake, null,
                               null, 0, null) == vpp.VPP_ERR_INVALID
     assert lib.vpp_selftest_wait_timeout(0, null) == vpp.VPP_ERR_INVALID
+    # fp8 cache: scales are required and 4-byte aligned
+    assert lib.vpp_kv_append_fp8(fake, fake, fake, fake, null, fake, fake, 2, 0, 29, 2, 128, 128,
+                                 null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_kv_append_fp8(fake, fake, fake, fake, bad, ctypes.c_void_p(0x100002), fake, 2, 0, 29, 2,
+                                 128, 128, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_kv_append_fp8(fake, fake, fake, fake, fake, fake, fake, 2, 0, 29, 2, 96, 128,
+                                 null) == vpp.VPP_ERR_UNSUPPORTED
+    assert lib.vpp_chunk_attn_fp8(fake, fake, fake, null, fake, fake, 2, 0, 29, 8, 2, 128, 128, 0.0, 0,
+                                  fake, null, fake, 1 << 30, null) == vpp.VPP_ERR_INVALID
+    # fp8 chunk attention: the widening needs a workspace
+    assert lib.vpp_chunk_attn_fp8(fake, fake, fake, fake, fake, fake, 2, 0, 29, 8, 2, 128, 128, 0.0, 0,
+                                  fake, null, null, 0, null) == vpp.VPP_ERR_WORKSPACE
+    assert lib.vpp_mixed_attn_fp8(fake, fake, fake, fake, null, fake, 4, 16, cu, ctx, 2, 8, 2, 128, 128,
+                                  0.0, fake, null, null, 0, null) == vpp.VPP_ERR_INVALID
+
+
+def test_fp8_workspace_sizes_are_host_side(lib):
+    # widened K and V of the visible keys (bf16), plus the split partials
+    P, C, H, Hkv, d = 1000, 200, 8, 2, 128
+    n = P + C
+    base = 2 * ((n * Hkv * d * 2 + 255) // 256 * 256)
+    assert vpp.chunk_attn_fp8_workspace_size(P, C, H, Hkv, d, d, 1) == base
+    assert vpp.chunk_attn_fp8_workspace_size(P, C, H, Hkv, d, d, 4) == \
+        base + vpp.chunk_attn_workspace_size(vpp.VPP_BF16, P, C, H, Hkv, d, d, 4)
+    # mixed: decode rows need no widening; the prefill sequence's whole context does
+    cu, ctx = [0, 1, 101], [5000, 400]
+    ws = vpp.mixed_attn_fp8_workspace_size(cu, ctx, H, Hkv, d, d)
+    assert ws == vpp.mixed_attn_workspace_size(cu, ctx, H, Hkv, d, d) + 2 * ((400 * Hkv * d * 2 + 255) // 256 * 256)
 
 
 def test_split_plan_is_host_side(lib):
