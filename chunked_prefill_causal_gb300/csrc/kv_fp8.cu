@@ -9,7 +9,7 @@
 // E4M3(code) x scale.
 //
 // Append: code = E4M3 round-to-nearest-even of the float32 quotient x / scale
-// (IEEE division), magnitudes above 448 clamped to 448.  A thread turns 16
+// (correctly rounded), magnitudes above 448 clamped to 448.  A thread turns 16
 // bf16 values (32 bytes) into 16 codes (one 16-byte store); HBM-bound:
 // 3 bytes per element (2 read, 1 written).
 //
@@ -24,8 +24,22 @@
 namespace vpp {
 namespace {
 
-// 16 bf16 values -> 16 E4M3 codes, each divided by s first.
-__device__ __forceinline__ uint4 quantise16(const uint4 a, const uint4 b, float s) {
+// x / s rounded to nearest even in float32, from y = RN(1/s): q = RN(x y) is
+// within one ulp of x / s, the residual x - q s is exact with an FMA, and
+// RN(q + (x - q s) y) is the correctly rounded quotient (Markstein's theorem
+// on Newton-Raphson division: P. Markstein, "IA-64 and Elementary Functions",
+// 2000; also Cornea, Harrison and Tang, 2002).  Quotients here stay far from
+// overflow and underflow (|x| <= bf16 range, scales are ordinary factors);
+// a zero x keeps its sign.
+__device__ __forceinline__ float div_rn(float x, float s, float y) {
+  const float q = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q, s, x);
+  const float q1 = __fmaf_rn(r, y, q);
+  return x == 0.f ? x : q1;
+}
+
+// 16 bf16 values -> 16 E4M3 codes, each divided by s first (y = RN(1/s)).
+__device__ __forceinline__ uint4 quantise16(const uint4 a, const uint4 b, float s, float y) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t out[4];
 #pragma unroll
@@ -33,8 +47,8 @@ __device__ __forceinline__ uint4 quantise16(const uint4 a, const uint4 b, float 
     const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
     const float x0 = __uint_as_float(w0 << 16), x1 = __uint_as_float(w0 & 0xFFFF0000u);
     const float x2 = __uint_as_float(w1 << 16), x3 = __uint_as_float(w1 & 0xFFFF0000u);
-    const uint32_t lo = pack_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-    const uint32_t hi = pack_e4m3x2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+    const uint32_t lo = pack_e4m3x2(div_rn(x0, s, y), div_rn(x1, s, y));
+    const uint32_t hi = pack_e4m3x2(div_rn(x2, s, y), div_rn(x3, s, y));
     out[i] = lo | (hi << 16);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
@@ -108,7 +122,7 @@ __device__ __forceinline__ void quantise_rows(const uint4* __restrict__ src, uin
       continue;
     }
     const float s = __ldg(scale + v / vec_per_head);
-    dst[row * vec_per_row + v] = quantise16(__ldg(&src[2 * i]), __ldg(&src[2 * i + 1]), s);
+    dst[row * vec_per_row + v] = quantise16(__ldg(&src[2 * i]), __ldg(&src[2 * i + 1]), s, __frcp_rn(s));
   }
 }
 

@@ -118,6 +118,28 @@ def test_append_codes_are_bit_exact():
     assert (cache.k[spare].cpu().numpy() == NAN_CODE).all()
 
 
+def test_append_codes_bit_exact_over_many_scales():
+    """8M elements per tensor, 64 kv heads with scales spread over eight decades (the
+    quotient x / scale must be the correctly rounded float32 one for every
+    code to agree)."""
+    Hkv, d, L = 64, 64, 2048
+    rng = np.random.default_rng(17)
+    k = gen((L, Hkv, d), 21, 1.0)
+    v = gen((L, Hkv, d), 22, 0.01)
+    ks = (10.0 ** rng.uniform(-5, 3, Hkv)).astype(np.float32)
+    vs = (10.0 ** rng.uniform(-7, 1, Hkv)).astype(np.float32)
+    kc = torch.full((L, Hkv, d), NAN_CODE, dtype=torch.uint8, device=DEV)
+    vc = torch.full((L, Hkv, d), NAN_CODE, dtype=torch.uint8, device=DEV)
+    vpp.vpp_kv_append_fp8(k.to(DEV), v.to(DEV), kc, vc, torch.from_numpy(ks).to(DEV),
+                          torch.from_numpy(vs).to(DEV), 0)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    for got, x, s in ((kc, k, ks), (vc, v, vs)):
+        ref = ofp8.quantize_kv(x.float().numpy(), s)
+        g = got.cpu().numpy()
+        assert np.array_equal(g, ref), (np.count_nonzero(g != ref), np.argwhere(g != ref)[:3])
+
+
 def test_append_contiguous_and_varlen_place_the_same_codes():
     Hkv, d = 2, 128
     ctx = np.array([100, 64, 1, 300], dtype=np.int32)
