@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture
 # (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "95f26535d9d78a08d9f1a2162a9e6ec99fc6d7a62cc4bef99f1c6c84c613ed86", "bytes_per_launch": 1.2167e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "9fe245498b942c2a82ff3b34ef1c2ac7fd60af4060c292cf663b6edab75794d4", "bytes_per_launch": 1.2233e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 

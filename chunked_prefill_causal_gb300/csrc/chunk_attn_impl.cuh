@@ -29,7 +29,8 @@
 //               while the tensor core works on the other tile's block, and the
 //               waits, commits and fences of one issuer (each leaves the tensor
 //               core idle if it sits between the MMAs of a single issuing
-//               thread) overlap the other issuer's MMAs.
+//               thread) overlap the other issuer's MMAs.  With d_qk = 192 the
+//               V tile is released right after its P V MMAs (see EARLY_V).
 //   warp 2      allocates and frees the 512 TMEM columns.
 //   warps 4-7   softmax + epilogue of query tile A; warps 8-11 of tile B.
 //               Each thread owns one query row = one TMEM lane, so row max and
@@ -84,6 +85,12 @@ struct Shape {
   static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_FULL = 10,
                        B_EMPTY = 10 + NB, NBARS = 10 + 2 * NB;
   static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
+  // With d_qk = 192 the ring holds under two K/V tile pairs, and the next K
+  // tile can only start once V_{j-1} is free: V_{j-1} is released by its own
+  // commit right after the P V MMAs rather than after the whole block (one
+  // more commit per block, which costs the d_qk = 128 shapes more than it
+  // gains them).
+  static constexpr bool EARLY_V = DQ > 128;
   static_assert(DV <= 128, "O accumulators must fit TMEM next to two S tiles");
   // Tile t of the load order (K_0, V_0, K_1, V_1, ...) starts at ring position
   // tile_pos(t) (counted in slots from the first tile, not wrapped).
@@ -345,6 +352,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         (j > 1 || k > 0) ? 1u : 0u);
             }
           }
+          if (S::EARLY_V) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         }
         if (j < n_kv) {
           // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_commit(bar(S::B_S + x));
           umma_commit(bar(S::B_EMPTY + tk % S::NB));
         }
-        if (j > 0) umma_commit(bar(S::B_EMPTY + tv % S::NB));
+        if (j > 0 && !S::EARLY_V) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         if (j == n_kv) umma_commit(bar(S::B_O + x));
       }
       if (!ok) {

@@ -4,7 +4,7 @@ This module holds no attention arithmetic.  It only draws inputs and lays out
 block tables, and both the CUDA path (tests, bench) and the CPU oracle read the
 same stored values from it.
 
-The five workloads mirror the pages' setups (cited by page title):
+The workloads mirror the pages' setups (cited by page title):
 
 * ``tiny``     -- 2 q heads / 1 kv head, head_dim 64, 512 tokens in 4 chunks
   of 128, float32 N(0,1), contiguous cache.
@@ -17,6 +17,8 @@ The five workloads mirror the pages' setups (cited by page title):
 * ``mla512k``  -- 128 heads, qk dim 192 (128 + 64 rope), v dim 128, 524288
   tokens in 24576-token chunks with a partial last chunk of 8192 (the
   DeepSeek-V3.1 512K runs with a 24K chunk budget, VPP review §3 and §4.6).
+* ``mla24k``   -- the mla512k head shapes on a 24576-token sequence in three
+  chunks of 8192: a case of a few GB that a profiler can capture whole.
 * ``mixed``    -- GQA 32 / 8, head_dim 128: four prefill chunks of 2048 tokens
   at prefixes {0, 16384, 65536, 122880} plus 256 decode rows whose context is
   uniform on [1024, 32768] ("Revisiting Pipeline Parallelism for LLM Serving",
@@ -71,6 +73,7 @@ WORKLOADS = {
     "gqa32k": Workload("gqa32k", 32, 8, 128, 128, 32768, 4096, "bf16", True, 2, 1 / math.sqrt(128)),
     "long128k": Workload("long128k", 64, 8, 128, 128, 131072, 16384, "bf16", True, 3, 1 / math.sqrt(128)),
     "mla512k": Workload("mla512k", 128, 128, 192, 128, 524288, 24576, "bf16", True, 4, 1 / math.sqrt(192)),
+    "mla24k": Workload("mla24k", 128, 128, 192, 128, 24576, 8192, "bf16", True, 7, 1 / math.sqrt(192)),
 }
 
 
