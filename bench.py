@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture
 # (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "9fe245498b942c2a82ff3b34ef1c2ac7fd60af4060c292cf663b6edab75794d4", "bytes_per_launch": 1.2233e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "779e9a3b1b03db0827bda04a36fab74d8ff732c1ee68b27a0ac52a2242dd6712", "bytes_per_launch": 1.2205e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 

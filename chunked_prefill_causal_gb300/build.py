@@ -39,13 +39,20 @@ def _stale(obj, src, hdr_mtime):
             or os.path.getmtime(obj) < hdr_mtime)
 
 
-def build(verbose: bool = False, jobs: int | None = None, extra_flags=()) -> str:
-    """Compiles what changed and (re)links libvpp.so; returns its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose: bool = False, jobs: int | None = None, extra_flags=(), out_dir: str | None = None,
+          lib_name: str = "libvpp.so") -> str:
+    """Compiles what changed and (re)links the library; returns its path.
+
+    The default is the product library, _build/libvpp.so.  A different
+    out_dir with extra_flags builds a variant beside it (the timeline build
+    of timeline.py) without touching the product's objects."""
+    out = out_dir or OUT_DIR
+    lib = os.path.join(out, lib_name)
+    os.makedirs(out, exist_ok=True)
     nvcc = _nvcc()
     hdr_mtime = max((os.path.getmtime(h) for h in _headers()), default=0.0)
     srcs = _sources()
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out, os.path.basename(s)[:-3] + ".o") for s in srcs]
     todo = [(s, o) for s, o in zip(srcs, objs) if _stale(o, s, hdr_mtime)]
 
     def compile_one(so):
@@ -64,14 +71,14 @@ def build(verbose: bool = False, jobs: int | None = None, extra_flags=()) -> str
             for s, err in ex.map(compile_one, todo):
                 if verbose and err:
                     sys.stderr.write(f"--- {os.path.basename(s)}\n{err}")
-    if todo or not os.path.exists(LIB) or any(os.path.getmtime(LIB) < os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+    if todo or not os.path.exists(lib) or any(os.path.getmtime(lib) < os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lpthread", "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

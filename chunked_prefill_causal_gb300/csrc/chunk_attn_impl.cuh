@@ -51,6 +51,21 @@
 #include "ptx.cuh"
 
 namespace vpp {
+
+// Timeline build only (-DVPP_TIMELINE=<cta>, see timeline.py): clock64 stamps
+// of the two MMA issuers and of the first softmax thread of each query tile,
+// for CTA 0 and CTA <cta>, tiles 0..63.  The product build compiles them out.
+#ifdef VPP_TIMELINE
+static __device__ long long g_timeline[2][4][64][4];
+__device__ __forceinline__ void timeline_stamp(int role, int j, int ev) {
+  const int slot = blockIdx.x == 0 ? 0 : (blockIdx.x == VPP_TIMELINE ? 1 : -1);
+  if (slot >= 0 && j < 64) g_timeline[slot][role][j][ev] = clock64();
+}
+#define VPP_STAMP(role, j, ev) timeline_stamp(role, j, ev)
+#else
+#define VPP_STAMP(role, j, ev) ((void)0)
+#endif
+
 namespace attn_detail {
 
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -314,6 +329,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!(ok = mbar_wait(bar(S::B_FULL + tv % S::NB), (tv / S::NB) & 1u, p.status, abort_flag))) break;
           if (!(ok = mbar_wait(bar(S::B_P + x), (j - 1) & 1, p.status, abort_flag))) break;
           tc_fence_after();
+          VPP_STAMP(x, j, 0);  // P of tile j-1 seen
         }
         if (j < n_kv &&
             !(ok = mbar_wait(bar(S::B_FULL + tk % S::NB), (tk / S::NB) & 1u, p.status, abort_flag)))
@@ -332,6 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           if (!ok) break;
         }
+        VPP_STAMP(x, j, 1);  // turn taken
         if (j > 0) {
           // O += P V for tile j-1 (P read from TMEM, V from the ring).
           if (S::NVC == 1 || vslot + S::NVC <= S::NSLOT) {
@@ -354,6 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           if (S::EARLY_V) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         }
+        VPP_STAMP(x, j, 3);  // P V issued
         if (j < n_kv) {
           // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
           // same TMEM columns, in issue order.
@@ -373,6 +391,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (j > 0 && !S::EARLY_V) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         if (j == n_kv) umma_commit(bar(S::B_O + x));
+        VPP_STAMP(x, j, 2);  // block issued
       }
       if (!ok) {
         *abort_flag = 1u;  // the partner issuer may be waiting for this turn
@@ -403,10 +422,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = warp_wait(bar(S::B_S + x), j & 1, p.status, abort_flag))) break;
       tc_fence_after();
+      if (row == 0) VPP_STAMP(2 + x, j, 0);  // S ready
       uint32_t u[4][32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32 * q, u[q]);
       tmem_ld_wait();
+      if (row == 0) VPP_STAMP(2 + x, j, 1);  // S in registers
       float sv[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(u[c >> 5][c & 31]);
@@ -495,9 +516,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           rs = exps_to_tmem(m);  // rows whose m did not move rewrite the same values
         }
       }
+      if (row == 0) VPP_STAMP(2 + x, j, 2);  // exponentials done
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(S::B_P + x));
+      if (row == 0) VPP_STAMP(2 + x, j, 3);  // P stored and signalled
       l += rs;
     }
     if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);

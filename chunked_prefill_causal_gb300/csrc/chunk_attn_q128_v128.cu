@@ -6,3 +6,14 @@ template cudaError_t launch_chunk_attn_t<128, 128>(const CUtensorMap&, const CUt
                                                 const CUtensorMap&, const AttnParams&, int,
                                                 cudaStream_t);
 }  // namespace vpp
+
+#ifdef VPP_TIMELINE
+// Timeline build only: copies out / clears the stamps of this instantiation.
+extern "C" int vpp_timeline_read(long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, vpp::g_timeline, sizeof(vpp::g_timeline)));
+}
+extern "C" int vpp_timeline_clear() {
+  static long long zero[2 * 4 * 64 * 4];
+  return static_cast<int>(cudaMemcpyToSymbol(vpp::g_timeline, zero, sizeof(zero)));
+}
+#endif
