@@ -481,9 +481,73 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
                                            round_up((size_t)items * heads * head_dim_v * 4, 256));
     }
     dp.status = ds->status;
-    if (launch_decode(dp, (int)items, head_dim_qk, fp8, ds->num_sms, st) != cudaSuccess)
+    if (launch_decode(dp, (int)items, head_dim_qk, fp8, false, ds->num_sms, st) != cudaSuccess)
       return VPP_ERR_CUDA;
   }
+  return VPP_OK;
+}
+
+// Top-k sparse prefix attention (DSA-style) of one chunk through the decode
+// kernel's gather mode: one work item per (token, range of 1024 list entries).
+size_t topk_ws_bytes(int64_t C, int32_t topk, int heads, int d) {
+  const int64_t S = ceil_div(topk, kDecodeSplitTokens);
+  if (S <= 1 || C <= 0) return 0;
+  return round_up((size_t)C * S * heads * d * 4, 256) + round_up((size_t)C * S * heads * 4, 256);
+}
+
+int topk_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+              const float* v_scale, const int32_t* block_table, int32_t num_blocks, int64_t P, int64_t C,
+              const int32_t* topk_idx, const int32_t* topk_len, int32_t topk, int heads, int kv_heads, int d,
+              float softmax_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+              cudaStream_t st) {
+  if (P < 0 || C < 0 || num_blocks <= 0 || topk < 1) return VPP_ERR_INVALID;
+  if (C == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
+  if (!q || !k_cache || !v_cache || !out || !topk_idx || !topk_len) return VPP_ERR_INVALID;
+  if (fp8 && !scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
+  if (int r = check_heads(heads, kv_heads)) return r;
+  if (!decode_supported(d, d, heads, kv_heads)) return VPP_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_len) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return VPP_ERR_INVALID;
+  if (block_table ? (int64_t)num_blocks * kBlockTokens < P + C : (int64_t)num_blocks < P + C)
+    return VPP_ERR_INVALID;
+  const int64_t S = ceil_div(topk, kDecodeSplitTokens);
+  const int64_t items = C * S;
+  if (items > INT32_MAX || C > INT32_MAX) return VPP_ERR_INVALID;
+  const size_t need = topk_ws_bytes(C, topk, heads, d);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return VPP_ERR_WORKSPACE;
+  DeviceState* ds = nullptr;
+  if (int r = device_state(&ds)) return r;
+  static DecodeParams zero_dp;
+  DecodeParams dp = zero_dp;
+  dp.heads = heads;
+  dp.kv_heads = kv_heads;
+  dp.split_tokens = kDecodeSplitTokens;
+  dp.num_blocks = num_blocks;
+  dp.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)d)) * 1.4426950408889634f;
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.k_cache = k_cache;
+  dp.v_cache = v_cache;
+  dp.k_scale = fp8 ? k_scale : nullptr;
+  dp.v_scale = fp8 ? v_scale : nullptr;
+  dp.block_table = block_table;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.lse = lse;
+  dp.lse_stride = C;
+  if (need > 0) {
+    dp.ws_o = static_cast<float*>(workspace);
+    dp.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         round_up((size_t)items * heads * d * 4, 256));
+  }
+  dp.status = ds->status;
+  dp.topk_idx = topk_idx;
+  dp.topk_len = topk_len;
+  dp.topk = topk;
+  dp.topk_splits = (int32_t)S;
+  dp.topk_prefix = P;
+  dp.topk_tokens = C;
+  if (launch_decode(dp, (int)items, d, fp8, true, ds->num_sms, st) != cudaSuccess) return VPP_ERR_CUDA;
   return VPP_OK;
 }
 
@@ -755,6 +819,34 @@ size_t vpp_mixed_attn_fp8_workspace_size(const int32_t* cu_seqlens_q, const int3
   if (check_heads(heads, kv_heads) != VPP_OK) return 0;
   return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v) +
          widen_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v);
+}
+
+// ------------------------------------------------------------- top-k sparse prefix
+int vpp_topk_chunk_attn(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        int32_t num_blocks, int64_t prefix_len, int64_t chunk_len, const int32_t* topk_idx,
+                        const int32_t* topk_len, int32_t topk, int heads, int kv_heads, int head_dim,
+                        float softmax_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  return topk_impl(false, q, k_cache, v_cache, nullptr, nullptr, block_table, num_blocks, prefix_len, chunk_len,
+                   topk_idx, topk_len, topk, heads, kv_heads, head_dim, softmax_scale, out, lse, workspace,
+                   workspace_bytes, as_stream(stream));
+}
+
+int vpp_topk_chunk_attn_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                            const float* v_scale, const int32_t* block_table, int32_t num_blocks,
+                            int64_t prefix_len, int64_t chunk_len, const int32_t* topk_idx,
+                            const int32_t* topk_len, int32_t topk, int heads, int kv_heads, int head_dim,
+                            float softmax_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
+  return topk_impl(true, q, k_cache, v_cache, k_scale, v_scale, block_table, num_blocks, prefix_len, chunk_len,
+                   topk_idx, topk_len, topk, heads, kv_heads, head_dim, softmax_scale, out, lse, workspace,
+                   workspace_bytes, as_stream(stream));
+}
+
+size_t vpp_topk_chunk_attn_workspace_size(int64_t chunk_len, int32_t topk, int heads, int head_dim) {
+  if (chunk_len <= 0 || topk < 1 || heads <= 0 || head_dim <= 0) return 0;
+  return topk_ws_bytes(chunk_len, topk, heads, head_dim);
 }
 
 int vpp_last_device_status(void* stream, int* code) {

@@ -29,6 +29,15 @@
 // fp8 cache (F8): the stages hold E4M3 codes, widened exactly to float in
 // registers; kv head h's k_scale joins its score scale and its v_scale
 // multiplies the output, so the cache bytes per row halve.
+//
+// Top-k mode (SP): the rows are the query tokens of one prefill chunk and each
+// attends only the key positions its index row lists (DSA-style sparse
+// attention: VPP technical review §7; "02 · 并行策略与 PP 切分" §5.1).  A work
+// item is (token, range of 1024 list entries).  The producer warp gathers a
+// step's 16 listed keys with one bulk copy per key for K and one for V (all kv
+// heads of a key are contiguous); entries outside 0 .. position, or in a block
+// outside the pool, are zero-filled, masked out of the softmax and reported as
+// VPP_ERR_INVALID.
 #include <algorithm>
 
 #include "common.cuh"
@@ -64,7 +73,7 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float* f) {
   f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, bool SP>
 __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int DPL = D / 8;     // score dims per lane (8 lanes per token)
   constexpr int OPL = D / 32;    // output dims per lane
@@ -77,21 +86,44 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
   float* pbuf = reinterpret_cast<float*>(smem + 196608);  // [hkv][16][G]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 196608 + 8 * kStepTokens * 8 * 4);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 16);
+  uint32_t* step_valid = reinterpret_cast<uint32_t*>(bars + 17);  // SP: valid-entry mask per stage
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------- work item
-  int lo = 0, hi = p.n_rows - 1;
   const int item = blockIdx.x;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.rows[mid].item0 <= item) lo = mid; else hi = mid - 1;
+  DecodeRow row;
+  int split, n_splits, t_begin, t_end;
+  const int32_t* list = nullptr;  // SP: this token's index row
+  int64_t pos = 0;                // SP: this token's absolute position
+  if (SP) {
+    const int64_t i = item / p.topk_splits;
+    split = item - static_cast<int>(i * p.topk_splits);
+    int n = __ldg(p.topk_len + i);
+    if (n < 1 || n > p.topk) {
+      if (threadIdx.x == 0 && split == 0) record_status(p.status, kStatusInvalid);
+      n = 0;
+    }
+    row.b = 0;
+    row.q_row = static_cast<int32_t>(i);
+    row.ctx = n;
+    row.item0 = static_cast<int32_t>(i * p.topk_splits);
+    list = p.topk_idx + i * p.topk;
+    pos = p.topk_prefix + i;
+    n_splits = n > 0 ? (n + p.split_tokens - 1) / p.split_tokens : 1;
+    if (split >= n_splits) return;  // the token's list is shorter: no work, nothing written
+  } else {
+    int lo = 0, hi = p.n_rows - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.rows[mid].item0 <= item) lo = mid; else hi = mid - 1;
+    }
+    row = p.rows[lo];
+    split = item - row.item0;
+    n_splits = (row.ctx + p.split_tokens - 1) / p.split_tokens;
   }
-  const DecodeRow row = p.rows[lo];
-  const int split = item - row.item0;
-  const int n_splits = (row.ctx + p.split_tokens - 1) / p.split_tokens;
-  const int t_begin = split * p.split_tokens;
-  const int t_end = min(row.ctx, t_begin + p.split_tokens);
+  t_begin = split * p.split_tokens;
+  t_end = min(row.ctx, t_begin + p.split_tokens);
   const int n_steps = (t_end - t_begin + kStepTokens - 1) / kStepTokens;
 
   if (threadIdx.x == 0) {
@@ -104,7 +136,69 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
   }
   __syncthreads();
 
-  if (warp == hkv) {
+  if (SP && warp == hkv) {
+    // ------------------------------------------------------ producer (gather)
+    // Lane t < 16 fetches the K row of list entry t0 + t, lane 16 + t its V row.
+    int slot = 0;
+    uint32_t phase = 0u;
+    uint32_t filled = 0u, fill_phase = 0u;
+    bool ok = true;
+    const int t = lane & 15;
+    const bool is_v = lane >= 16;
+    for (int s = 0; s < n_steps; ++s) {
+      const int t0 = t_begin + s * kStepTokens;
+      const int nt = min(kStepTokens, t_end - t0);
+      bool valid = false;
+      int64_t src_row = 0;
+      if (t < nt) {
+        const int64_t key = __ldg(list + t0 + t);
+        if (key >= 0 && key <= pos) {
+          if (p.block_table) {
+            const int32_t blk = __ldg(p.block_table + key / kBlockTokens);
+            valid = blk >= 0 && blk < p.num_blocks;
+            src_row = static_cast<int64_t>(blk) * kBlockTokens + key % kBlockTokens;
+          } else {
+            valid = key < p.num_blocks;  // contiguous cache: num_blocks is the capacity in tokens
+            src_row = key;
+          }
+        }
+        if (!valid && !is_v) record_status(p.status, kStatusInvalid);
+      }
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;  // K lanes decide
+      bool w_ok = true;
+      if (lane == 0) w_ok = mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag);
+      if (!__shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? kStepTokens * row_bytes : 0) + t * row_bytes;
+      if (t < nt && !valid) {  // zero-filled, so that P = 0 times it stays 0
+        for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();  // before later bulk copies into these bytes
+      }
+      __syncwarp();
+      const uint32_t full = smem_u32(&bars[slot]);
+      if (lane == 0) {
+        step_valid[slot] = vmask;
+        mbar_arrive_expect_tx(full, 2u * static_cast<uint32_t>(__popc(vmask)) * row_bytes);
+      }
+      __syncwarp();
+      if (t < nt && valid) {
+        const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
+        bulk_g2s(smem_u32(dstp), base + src_row * row_bytes, static_cast<uint32_t>(row_bytes), full);
+      }
+      filled |= 1u << slot;
+      fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
+      if (++slot == nstage) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int i = 0; i < nstage; ++i)
+        if (filled & (1u << i)) mbar_wait_for(smem_u32(&bars[i]), (fill_phase >> i) & 1u, 100000000ull);
+    }
+  } else if (warp == hkv) {
     // ------------------------------------------------------ producer
     if (lane == 0) {
       int slot = 0;
@@ -187,6 +281,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
       if (!ok) break;
       const uint8_t* kst = smem + slot * stage_bytes;
       const uint8_t* vst = kst + kStepTokens * row_bytes;
+      const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
       // Scores of this step's 16 tokens (4 passes of 4 tokens).
       float sc[4][G];
 #pragma unroll
@@ -229,7 +324,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
           v += __shfl_xor_sync(0xffffffffu, v, 4);
-          sc[ps][j] = (t < nt) ? v * sl : -INFINITY;
+          sc[ps][j] = (t < nt && ((vmask >> t) & 1u)) ? v * sl : -INFINITY;
         }
       }
       // Online softmax, per query head.
@@ -238,7 +333,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float mx = fmax3(fmaxf(sc[0][j], sc[1][j]), sc[2][j], sc[3][j]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        if (mx > m[j] + 8.0f || m[j] == -INFINITY) {  // warp-uniform
+        if (mx > m[j] + 8.0f || (m[j] == -INFINITY && mx != -INFINITY)) {  // warp-uniform
           const float f = (m[j] == -INFINITY) ? 0.f : ex2_approx(m[j] - mx);
           lpart[j] *= f;
 #pragma unroll
@@ -248,7 +343,8 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float ps_sum = 0.f;
 #pragma unroll
         for (int ps = 0; ps < 4; ++ps) {
-          const float pv = ex2_approx(sc[ps][j] - m[j]);
+          // (a top-k step may hold no valid entry before any valid one: m = -inf)
+          const float pv = (SP && m[j] == -INFINITY) ? 0.f : ex2_approx(sc[ps][j] - m[j]);
           ps_sum += pv;
           if (r == 0) pw[(4 * ps + tt) * G + j] = pv;
         }
@@ -313,8 +409,9 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float l = lpart[j];
 #pragma unroll
         for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
-        const float inv = vsc / l;
-        const float lse_v = m[j] * kLn2d + logf(l);
+        const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
+        const float inv = empty ? 0.f : vsc / l;
+        const float lse_v = empty ? -INFINITY : m[j] * kLn2d + logf(l);
         const int hq = h * G + j;
         if (n_splits == 1) {
           uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + lane * OPL;
@@ -337,15 +434,25 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
 }
 
 // Combines the ranges of every multi-range row: one warp per (row, head).
-template <int D>
+template <int D, bool SP>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int OPL = D / 32;
   const int lane = threadIdx.x & 31;
-  const int64_t n = static_cast<int64_t>(p.n_rows) * p.heads;
+  const int64_t n = (SP ? p.topk_tokens : static_cast<int64_t>(p.n_rows)) * p.heads;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n;
        w += wstride) {
-    const DecodeRow row = p.rows[w / p.heads];
+    DecodeRow row;
+    if (SP) {
+      const int64_t i = w / p.heads;
+      int len = __ldg(p.topk_len + i);
+      if (len < 1 || len > p.topk) len = 0;
+      row.q_row = static_cast<int32_t>(i);
+      row.ctx = len;
+      row.item0 = static_cast<int32_t>(i * p.topk_splits);
+    } else {
+      row = p.rows[w / p.heads];
+    }
     const int hq = static_cast<int>(w % p.heads);
     const int ns = (row.ctx + p.split_tokens - 1) / p.split_tokens;
     if (ns <= 1) continue;
@@ -354,6 +461,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
       mx = fmaxf(mx, p.ws_lse[(static_cast<int64_t>(row.item0) + s) * p.heads + hq]);
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+    if (mx == -INFINITY) mx = 0.f;  // every range empty: weights 0, output 0, lse -inf
     float acc[OPL];
 #pragma unroll
     for (int i = 0; i < OPL; ++i) acc[i] = 0.f;
@@ -366,7 +474,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 #pragma unroll
       for (int i = 0; i < OPL; ++i) acc[i] += wgt * src[i];
     }
-    const float inv = 1.f / tot;
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
     uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + lane * OPL;
     if (OPL == 4) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1 % OPL] * inv),
@@ -374,29 +482,30 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
     } else {
       *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % OPL] * inv);
     }
-    if (p.lse && lane == 0) p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = mx + logf(tot);
+    if (p.lse && lane == 0)
+      p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
   }
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, bool SP>
 cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t st) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<D, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<D, G, F8, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kDecodeSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  decode_kernel<D, G, F8><<<items, 32 * (p.kv_heads + 1), kDecodeSmem, st>>>(p);
+  decode_kernel<D, G, F8, SP><<<items, 32 * (p.kv_heads + 1), kDecodeSmem, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int grid = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(p.n_rows) * p.heads + 7) / 8,
-                                                static_cast<int64_t>(num_sms) * 16));
+  const int64_t rows = SP ? p.topk_tokens : static_cast<int64_t>(p.n_rows);
+  int grid = static_cast<int>(std::min<int64_t>((rows * p.heads + 7) / 8, static_cast<int64_t>(num_sms) * 16));
   if (grid < 1) grid = 1;
-  decode_merge_kernel<D><<<grid, 256, 0, st>>>(p);
+  decode_merge_kernel<D, SP><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -410,26 +519,29 @@ bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads) 
   return g == 1 || g == 2 || g == 4 || (g == 8 && head_dim_qk == 64);
 }
 
-template <bool F8>
+template <bool F8, bool SP>
 cudaError_t launch_f(const DecodeParams& p, int items, int head_dim, int num_sms, cudaStream_t stream) {
   const int g = p.heads / p.kv_heads;
   if (head_dim == 128) {
-    if (g == 1) return launch_t<128, 1, F8>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<128, 2, F8>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<128, 4, F8>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<128, 1, F8, SP>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<128, 2, F8, SP>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<128, 4, F8, SP>(p, items, num_sms, stream);
   } else if (head_dim == 64) {
-    if (g == 1) return launch_t<64, 1, F8>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<64, 2, F8>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<64, 4, F8>(p, items, num_sms, stream);
-    if (g == 8) return launch_t<64, 8, F8>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<64, 1, F8, SP>(p, items, num_sms, stream);
+    if (g == 2) return launch_t<64, 2, F8, SP>(p, items, num_sms, stream);
+    if (g == 4) return launch_t<64, 4, F8, SP>(p, items, num_sms, stream);
+    if (g == 8) return launch_t<64, 8, F8, SP>(p, items, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, int num_sms,
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, bool topk, int num_sms,
                           cudaStream_t stream) {
-  return fp8 ? launch_f<true>(p, items, head_dim, num_sms, stream)
-             : launch_f<false>(p, items, head_dim, num_sms, stream);
+  if (topk)
+    return fp8 ? launch_f<true, true>(p, items, head_dim, num_sms, stream)
+               : launch_f<false, true>(p, items, head_dim, num_sms, stream);
+  return fp8 ? launch_f<true, false>(p, items, head_dim, num_sms, stream)
+             : launch_f<false, false>(p, items, head_dim, num_sms, stream);
 }
 
 }  // namespace vpp

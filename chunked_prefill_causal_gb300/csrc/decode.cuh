@@ -37,6 +37,15 @@ struct DecodeParams {
   float* ws_o;                 // float32 [items][heads][d] partials
   float* ws_lse;               // [items][heads]
   int* status;
+  // Top-k mode (topk_idx != null): query token i of one chunk (prefix
+  // topk_prefix) attends the key positions topk_idx[i][0 .. topk_len[i]-1]
+  // of the sequence in block-table row 0; rows[] and n_rows are unused.
+  const int32_t* topk_idx;     // [n_tokens][topk]
+  const int32_t* topk_len;     // [n_tokens]
+  int32_t topk;                // row stride of topk_idx (the list capacity k)
+  int32_t topk_splits;         // work items per token: ceil(k / split_tokens)
+  int64_t topk_prefix;
+  int64_t topk_tokens;
   DecodeRow rows[kMaxBatch];
 };
 
@@ -48,7 +57,8 @@ constexpr int kDecodeSplitTokens = 1024;
 bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads);
 
 // fp8: the cache holds E4M3 codes with per-kv-head k_scale / v_scale.
-cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, int num_sms,
+// topk: p.topk_idx rows instead of decode rows (items = tokens x topk_splits).
+cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, bool topk, int num_sms,
                           cudaStream_t stream);
 
 }  // namespace vpp

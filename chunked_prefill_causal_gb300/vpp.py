@@ -55,6 +55,12 @@ SIGNATURES = {
                             _c_void_p, _c_void_p, _i32, _int, _int, _int, _int, _f32, _c_void_p, _c_void_p,
                             _c_void_p, _sz, _c_void_p], _int),
     "vpp_mixed_attn_fp8_workspace_size": ([_c_void_p, _c_void_p, _i32, _int, _int, _int, _int], _sz),
+    "vpp_topk_chunk_attn": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64, _i64, _c_void_p, _c_void_p,
+                             _i32, _int, _int, _int, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p], _int),
+    "vpp_topk_chunk_attn_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64,
+                                 _i64, _c_void_p, _c_void_p, _i32, _int, _int, _int, _f32, _c_void_p, _c_void_p,
+                                 _c_void_p, _sz, _c_void_p], _int),
+    "vpp_topk_chunk_attn_workspace_size": ([_i64, _i32, _int, _int], _sz),
     "vpp_last_device_status": ([_c_void_p, ctypes.POINTER(_int)], _int),
     "vpp_selftest_wait_timeout": ([_int, _c_void_p], _int),
 }
@@ -353,6 +359,59 @@ def vpp_mixed_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, cu_se
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
         block_table.shape[1], k_cache.shape[0], cu_p, ctx_p, len(ctx), H, Hkv, dq, dv, float(softmax_scale),
         _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- top-k sparse prefix
+def topk_chunk_attn_workspace_size(chunk_len, topk, heads, head_dim):
+    return int(load().vpp_topk_chunk_attn_workspace_size(int(chunk_len), int(topk), heads, head_dim))
+
+
+def _topk_args(q, k_cache, topk_idx, topk_len, workspace):
+    if topk_idx.dtype != torch.int32 or topk_len.dtype != torch.int32:
+        raise ValueError("topk_idx and topk_len are int32")
+    C, H, d = q.shape
+    topk = topk_idx.shape[1]
+    if topk_idx.shape[0] != C or topk_len.shape[0] != C:
+        raise ValueError("one index row and one length per query token")
+    if workspace is None:
+        need = topk_chunk_attn_workspace_size(C, topk, H, d)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return C, H, d, topk, workspace, wbytes
+
+
+def vpp_topk_chunk_attn(q, k_cache, v_cache, prefix_len, topk_idx, topk_len, block_table=None, out=None, lse=None,
+                        softmax_scale=0.0, workspace=None, stream=None):
+    """Top-k sparse prefix attention of a chunk (bf16 q and cache): query token i
+    attends the key positions topk_idx[i, :topk_len[i]] (int32 CUDA tensors)."""
+    _need_cuda(q, k_cache, v_cache, topk_idx, topk_len, block_table, out, lse, workspace)
+    C, H, d, topk, workspace, wbytes = _topk_args(q, k_cache, topk_idx, topk_len, workspace)
+    Hkv = k_cache.shape[-2]
+    if out is None:
+        out = torch.empty((C, H, d), dtype=torch.bfloat16, device=q.device)
+    _check("vpp_topk_chunk_attn", load().vpp_topk_chunk_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), k_cache.shape[0], int(prefix_len), C,
+        _ptr(topk_idx), _ptr(topk_len), topk, H, Hkv, d, float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), wbytes, _stream(stream)))
+    return out
+
+
+def vpp_topk_chunk_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, prefix_len, topk_idx, topk_len,
+                            block_table=None, out=None, lse=None, softmax_scale=0.0, workspace=None, stream=None):
+    """vpp_topk_chunk_attn over an E4M3 cache (uint8 codes, per-kv-head scales)."""
+    _need_cuda(q, k_cache, v_cache, topk_idx, topk_len, block_table, out, lse, workspace)
+    _fp8_cache(k_cache, v_cache)
+    C, H, d, topk, workspace, wbytes = _topk_args(q, k_cache, topk_idx, topk_len, workspace)
+    Hkv = k_cache.shape[-2]
+    _scales(k_scale, v_scale, Hkv)
+    if out is None:
+        out = torch.empty((C, H, d), dtype=torch.bfloat16, device=q.device)
+    _check("vpp_topk_chunk_attn_fp8", load().vpp_topk_chunk_attn_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), k_cache.shape[0],
+        int(prefix_len), C, _ptr(topk_idx), _ptr(topk_len), topk, H, Hkv, d, float(softmax_scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), wbytes, _stream(stream)))
     return out
 
 

@@ -19,6 +19,9 @@ The workloads mirror the pages' setups (cited by page title):
   DeepSeek-V3.1 512K runs with a 24K chunk budget, VPP review §3 and §4.6).
 * ``mla24k``   -- the mla512k head shapes on a 24576-token sequence in three
   chunks of 8192: a case of a few GB that a profiler can capture whole.
+* ``dsa128k``  -- GQA 32 / 8, head_dim 128, 131072 tokens in 8 chunks of
+  16384, for top-k sparse prefix attention: every query token lists up to
+  ``TOPK`` earlier keys (DSA-style, VPP technical review §7).
 * ``mixed``    -- GQA 32 / 8, head_dim 128: four prefill chunks of 2048 tokens
   at prefixes {0, 16384, 65536, 122880} plus 256 decode rows whose context is
   uniform on [1024, 32768] ("Revisiting Pipeline Parallelism for LLM Serving",
@@ -74,7 +77,44 @@ WORKLOADS = {
     "long128k": Workload("long128k", 64, 8, 128, 128, 131072, 16384, "bf16", True, 3, 1 / math.sqrt(128)),
     "mla512k": Workload("mla512k", 128, 128, 192, 128, 524288, 24576, "bf16", True, 4, 1 / math.sqrt(192)),
     "mla24k": Workload("mla24k", 128, 128, 192, 128, 24576, 8192, "bf16", True, 7, 1 / math.sqrt(192)),
+    "dsa128k": Workload("dsa128k", 32, 8, 128, 128, 131072, 16384, "bf16", True, 8, 1 / math.sqrt(128)),
 }
+
+# Listed keys per query token of the top-k (DSA-style) workloads; the pages
+# give no value, 2048 is the reading.
+TOPK = 2048
+
+
+def topk_indices(prefix_len: int, chunk_len: int, topk: int = TOPK, seed: int = 0, device="cpu"):
+    """Synthetic top-k key lists of a chunk's query tokens (seeded).
+
+    Token i sits at p = prefix_len + i.  If p + 1 <= topk it lists every key
+    0 .. p; otherwise it lists one key drawn uniformly from each of topk - 1
+    equal strata of 0 .. p - 1, then p itself (so the entries are distinct
+    and spread over the whole prefix).  Returns int32 torch tensors on
+    ``device``: idx [C, topk] with the valid entries first and -1 padding,
+    and lens [C].  The draws come from a torch generator on ``device``, so a
+    seed gives one list on CPU and another on a GPU.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1_000_003 + 17)
+    C = int(chunk_len)
+    pos = int(prefix_len) + torch.arange(C, dtype=torch.int64, device=device)
+    lens = torch.clamp(pos + 1, max=topk)
+    ar = torch.arange(topk, dtype=torch.int64, device=device)
+    idx = torch.where(ar[None, :] <= pos[:, None], ar[None, :].expand(C, topk), torch.full_like(ar[None, :], -1))
+    sparse = pos + 1 > topk
+    if bool(sparse.any()):
+        rows = torch.nonzero(sparse).squeeze(1)
+        ps = pos[rows][:, None]
+        m = topk - 1
+        j = torch.arange(m, dtype=torch.int64, device=device)[None, :]
+        lo = (j * ps) // m
+        hi = ((j + 1) * ps) // m
+        u = torch.rand((rows.numel(), m), generator=g, device=device, dtype=torch.float64)
+        picks = lo + torch.floor(u * (hi - lo).to(torch.float64)).to(torch.int64)
+        idx[rows] = torch.cat([picks, ps], dim=1)
+    return idx.to(torch.int32), lens.to(torch.int32)
 
 
 @dataclasses.dataclass(frozen=True)

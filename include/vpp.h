@@ -319,6 +319,52 @@ size_t vpp_mixed_attn_fp8_workspace_size(const int32_t *cu_seqlens_q,
                                          int head_dim_v);
 
 /*
+ * Top-k sparse prefix attention (DSA-style): [VPP review] §7 (sparse attention
+ * breaks the linear per-chunk latency law) and [GLM PP note] §5.1 (an indexer
+ * selects top-k earlier tokens for every query token; the main attention
+ * reads only those).  The indexer is not part of this library: the indices
+ * are inputs.
+ *
+ * Query token i of the chunk (absolute position prefix_len + i) attends the
+ * key positions topk_idx[i][0 .. topk_len[i]-1] (DEVICE int32, row stride
+ * topk, each row's valid entries first), with the same list for every head:
+ *   out[i][h] = softmax_j(q[i][h] . k[j][h/G] * scale) v[j][h/G] over the list,
+ * a position listed twice counting twice; lse as in vpp_chunk_attn_ex.
+ * Entries outside 0 .. prefix_len + i, or in a block outside the pool, are
+ * left out of the softmax and reported as VPP_ERR_INVALID in the status word;
+ * a row with no usable entry (or topk_len outside 1 .. topk) gets out = 0 and
+ * lse = -inf.  Cache: bf16, paged (block_table of the one sequence) or
+ * contiguous (block_table NULL, num_blocks = capacity in tokens); the keys up
+ * to prefix_len + chunk_len - 1 must be in it.  Shapes: those of the decode
+ * kernel (head_dim 64 or 128, kv_heads <= 8, heads/kv_heads 1, 2, 4, or 8
+ * with head_dim 64); others return VPP_ERR_UNSUPPORTED.  workspace >=
+ * vpp_topk_chunk_attn_workspace_size(...) (0 when topk <= 1024).
+ */
+int vpp_topk_chunk_attn(const void *q, const void *k_cache,
+                        const void *v_cache, const int32_t *block_table,
+                        int32_t num_blocks, int64_t prefix_len,
+                        int64_t chunk_len, const int32_t *topk_idx,
+                        const int32_t *topk_len, int32_t topk, int heads,
+                        int kv_heads, int head_dim, float softmax_scale,
+                        void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* The same over an fp8 (E4M3) cache with per-kv-head scales (see above). */
+int vpp_topk_chunk_attn_fp8(const void *q, const void *k_cache,
+                            const void *v_cache, const float *k_scale,
+                            const float *v_scale, const int32_t *block_table,
+                            int32_t num_blocks, int64_t prefix_len,
+                            int64_t chunk_len, const int32_t *topk_idx,
+                            const int32_t *topk_len, int32_t topk, int heads,
+                            int kv_heads, int head_dim, float softmax_scale,
+                            void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of vpp_topk_chunk_attn / _fp8 (key-range partials). */
+size_t vpp_topk_chunk_attn_workspace_size(int64_t chunk_len, int32_t topk,
+                                          int heads, int head_dim);
+
+/*
  * Device status word: synchronises `stream`, stores the first error any
  * kernel of this library recorded since the last reset (VPP_OK if none) in
  * *code, and resets the word to VPP_OK.  Returns VPP_ERR_CUDA if the

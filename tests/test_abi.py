@@ -87,6 +87,25 @@ def test_host_validation_rejects_bad_arguments(lib):
                                   0.0, fake, null, null, 0, null) == vpp.VPP_ERR_INVALID
 
 
+def test_topk_validation_and_workspace(lib):
+    null = None
+    fake = ctypes.c_void_p(0x100000)
+    # no index list / unsupported shape (d 128 with 8 query heads per kv head) / bad topk
+    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, null, fake, 2048, 8, 2, 128, 0.0, fake,
+                                   null, null, 0, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 2048, 64, 8, 128, 0.0, fake,
+                                   null, null, 0, null) == vpp.VPP_ERR_UNSUPPORTED
+    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 0, 8, 2, 128, 0.0, fake,
+                                   null, null, 0, null) == vpp.VPP_ERR_INVALID
+    # more than 1024 entries per list: key-range partials need a workspace
+    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 2048, 8, 2, 128, 0.0, fake,
+                                   null, null, 0, null) == vpp.VPP_ERR_WORKSPACE
+    assert vpp.topk_chunk_attn_workspace_size(16, 1024, 8, 128) == 0
+    assert vpp.topk_chunk_attn_workspace_size(16, 2048, 8, 128) == 16 * 2 * 8 * 128 * 4 + 16 * 2 * 8 * 4
+    assert lib.vpp_topk_chunk_attn_fp8(fake, fake, fake, null, fake, fake, 64, 0, 16, fake, fake, 1024, 8, 2, 128,
+                                       0.0, fake, null, null, 0, null) == vpp.VPP_ERR_INVALID
+
+
 def test_fp8_workspace_sizes_are_host_side(lib):
     # widened K and V of the visible keys (bf16), plus the split partials
     P, C, H, Hkv, d = 1000, 200, 8, 2, 128
