@@ -446,6 +446,50 @@ def measure_fp8(dev, stream, hbm, w, chunks):
     return out
 
 
+def measure_topk(dev, stream, hbm, peak_tf):
+    """Top-k sparse prefix attention (DSA-style) on the dsa128k workload
+    (32/8 heads, d 128, 8 chunks of 16384, TOPK listed keys per query token)
+    against dense chunk attention on the same shapes, and the two-rank
+    schedules simulated on each set of per-chunk latencies."""
+    from chunked_prefill_causal_gb300 import vpp
+    w = W.WORKLOADS["dsa128k"]
+    chunks = w.chunks()
+    nb = W.blocks_for(w.seq_len)
+    table = torch.from_numpy(W.block_table(nb, nb + 8, w.seed + 99)).to(dev)
+    kc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    qs = []
+    for ci, (p0, c0) in enumerate(chunks):
+        qi, ki, vi = W.chunk_tensors(w, ci, dev)
+        vpp.vpp_kv_append(ki, vi, kc, vc, p0, block_table=table)
+        qs.append(qi)
+        del ki, vi
+    out = torch.empty((w.chunk, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    ws_t = torch.empty(max(vpp.topk_chunk_attn_workspace_size(w.chunk, W.TOPK, w.heads, w.head_dim_qk), 256),
+                       dtype=torch.uint8, device=dev)
+    rows, sparse_ms, dense_ms = [], [], []
+    for ci, (P, C) in enumerate(chunks):
+        idx, lens = W.topk_indices(P, C, W.TOPK, ci, device=dev)
+        ts = time_events(lambda: vpp.vpp_topk_chunk_attn(qs[ci], kc, vc, P, idx, lens, block_table=table,
+                                                         out=out[:C], workspace=ws_t), 5, stream)
+        td = time_events(lambda: vpp.vpp_chunk_attn_ex(qs[ci], kc, vc, P, block_table=table, out=out[:C],
+                                                       num_splits=1), 3, stream)
+        n_listed = int(lens.to(torch.int64).sum())
+        byts = n_listed * w.kv_heads * (w.head_dim_qk + w.head_dim_v) * 2
+        fl = 2.0 * (w.head_dim_qk + w.head_dim_v) * w.heads * n_listed
+        dfl = 2.0 * (w.head_dim_qk + w.head_dim_v) * w.heads * (C * P + C * (C + 1) // 2)
+        sparse_ms.append(ts)
+        dense_ms.append(td)
+        rows.append({"k": ci, "prefix": P, "sparse_ms": round(ts, 3), "dense_ms": round(td, 3),
+                     "gathered_gb": round(byts / 1e9, 2), "sparse_gbs": round(byts / (ts / 1e3) / 1e9, 1),
+                     "sparse_frac_hbm": round(byts / (ts / 1e3) / 1e9 / hbm, 4),
+                     "sparse_tflops": round(fl / (ts / 1e3) / 1e12, 1),
+                     "dense_tflops": round(dfl / (td / 1e3) / 1e12, 1)})
+    return {"workload": f"dsa128k: 32/8 heads, d 128, 8 chunks of 16384, {W.TOPK} listed keys per query token",
+            "per_chunk": rows,
+            "schedule_dense": schedule_summary(dense_ms), "schedule_sparse": schedule_summary(sparse_ms)}
+
+
 def measure_cost_model(dev, stream, n_batches=48, n_train=32, seed=11):
     """Times random mixed micro-batches through vpp_mixed_attn and fits the
     micro-batch latency model (cost_model.py) to them: MAPE on held-out
@@ -736,6 +780,8 @@ def run_ours(args, dist_):
         extras["cost_model"] = measure_cost_model(dev, stream)
         torch.cuda.empty_cache()
         extras["fp8_kv"] = measure_fp8(dev, stream, hbm, w, chunks)
+        torch.cuda.empty_cache()
+        extras["topk_sparse"] = measure_topk(dev, stream, hbm, peak_tf)
 
     if dist_.rank == 0:
         line = {
