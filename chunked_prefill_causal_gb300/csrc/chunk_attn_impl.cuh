@@ -70,8 +70,8 @@ namespace attn_detail {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
-constexpr int kRegsLow = 72;
-constexpr int kRegsHigh = 216;
+constexpr int kRegsLow = 112;
+constexpr int kRegsHigh = 192;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch");
 constexpr uint64_t kCleanupNs = 100000000ull;  // 0.1 s for clean-up waits after an abort
 
@@ -437,15 +437,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (key0 + c > lim) sv[c] = -INFINITY;
       }
-      // Row max (eight independent chains of 3-input max, then a tree).
+      // Row max: eight independent chains of 3-input max, then a tree.  Chain
+      // i takes sv[i] and pairs sv[c + 2i], sv[c + 2i + 1] for c = 8 .. 104;
+      // in the last step (sv[120..127], four pairs) chains i and i + 4 take the
+      // same pair, which leaves the maximum unchanged.
       auto row_max = [&]() {
         float mx8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-        for (int c = 8; c < 128; c += 16)
+        for (int c = 8; c + 16 <= 128; c += 16)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[120 + 2 * (i & 3)], sv[121 + 2 * (i & 3)]);
         return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                      fmaxf(mx8[6], mx8[7]));
       };
