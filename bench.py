@@ -134,11 +134,14 @@ class Dist:
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = False
+        self.backend = None
 
-    def init(self, backend="nccl"):
+    def init(self, backend=None):
+        """One process group per job: NCCL when the rank has a GPU, gloo otherwise."""
         if self.world > 1 and not self.pg:
             import torch.distributed as dist
-            dist.init_process_group(backend)
+            self.backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+            dist.init_process_group(self.backend)
             self.pg = True
 
     def barrier(self):
@@ -147,10 +150,11 @@ class Dist:
             dist.barrier()
 
     def max(self, x: float) -> float:
+        """The maximum of x over all ranks (the job's time is its slowest rank's)."""
         if not self.pg:
             return x
         import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if self.backend == "nccl" else "cpu")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
