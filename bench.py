@@ -828,24 +828,28 @@ def run_mixed(args, dist_):
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     stream = torch.cuda.current_stream()
-    ms = MixedSetup(dev, args.decode_rows)
+    fp8 = args.kv_dtype == "fp8"
+    ms = MixedSetup(dev, args.decode_rows, fp8=fp8)
+    step = ms.step_fp8 if fp8 else ms.step
+    decode_only = ms.decode_only_fp8 if fp8 else ms.decode_only
     for _ in range(args.warmup):
-        ms.step()
+        step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     dist_.barrier()
     e0.record(stream)
     for _ in range(args.steps):
-        ms.step()
+        step()
     e1.record(stream)
     torch.cuda.synchronize()
     dist_.barrier()
     if vpp.vpp_last_device_status() != 0:
         raise RuntimeError("device status word reported an error")
     el = dist_.max(e0.elapsed_time(e1) / 1e3)
-    dec_ms = time_events(ms.decode_only, 5, stream)
-    gbs = ms.decode_bytes / (dec_ms / 1e3) / 1e9
+    dec_ms = time_events(decode_only, 5, stream)
+    dec_bytes = ms.decode_bytes // 2 if fp8 else ms.decode_bytes  # one byte per cached element
+    gbs = dec_bytes / (dec_ms / 1e3) / 1e9
     if dist_.rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": (ms.prefill_flops + ms.decode_flops) * args.steps * dist_.world / el / 1e12,
@@ -853,7 +857,7 @@ def run_mixed(args, dist_):
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "mixed", "decode_rows": len(ms.ctx_d), "heads": 32, "kv_heads": 8,
-                       "head_dim": 128},
+                       "head_dim": 128, "kv_cache": "E4M3 codes, per-kv-head scales" if fp8 else "bf16"},
             "decode_only_ms": round(dec_ms, 3), "decode_gbs": round(gbs, 1),
             "decode_frac_hbm": round(gbs / hbm, 4), "hbm_peak_source": pk_src}), flush=True)
     return 0
@@ -872,6 +876,8 @@ def main(argv=None):
                     help="skip the KV-append and mixed-batch measurements")
     ap.add_argument("--decode-rows", type=int, default=None,
                     help="with --workload mixed: decode rows of the micro-batch (default 256)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="with --workload mixed: the KV cache's element type")
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=256)

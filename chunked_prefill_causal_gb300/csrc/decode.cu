@@ -26,9 +26,12 @@
 // them ("02 · 并行策略与 PP 切分" note, §7).  HBM-bound: the algorithmic bytes
 // are ctx x Hkv x (dq + dv) x 2 per row plus q, out and the partials.
 //
-// fp8 cache (F8): the stages hold E4M3 codes, widened exactly to float in
-// registers; kv head h's k_scale joins its score scale and its v_scale
-// multiplies the output, so the cache bytes per row halve.
+// fp8 cache (F8): the stages hold E4M3 codes, and both products run on the
+// tensor cores (warp-level mma.sync, f16 operands: every
+// E4M3 value is an f16 value; f32 accumulation), which takes the per-element
+// widening and the G multiply-adds per key off the CUDA cores.  kv head h's
+// k_scale joins its score scale and its v_scale multiplies the output, so
+// the cache bytes per row halve.
 //
 // Top-k mode (SP): the rows are the query tokens of one prefill chunk and each
 // attends only the key positions its index row lists (DSA-style sparse
@@ -48,7 +51,10 @@ namespace vpp {
 namespace {
 
 constexpr int kStepTokens = 16;
-constexpr int kDecodeSmem = 196608 + 4096 + 256;  // ring + p exchange + barriers
+// Stage ring: six fp8 stages (32 rows of 1 KB + 128 bytes of group padding)
+// or three bf16 stages of 64 KB, for 8 kv heads of d 128.
+constexpr int kDecodeRing = 6 * (32 * 1024 + 128);
+constexpr int kDecodeSmem = kDecodeRing + 4096 + 256;  // ring + p exchange + barriers
 constexpr float kLn2d = 0.69314718055994530942f;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -63,14 +69,38 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// 8 E4M3 codes -> 8 floats (exact).
-__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float* f) {
-  const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w.x & 0xFFFFu));
-  const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w.x >> 16));
-  const float2 c = e4m3x2_to_f32x2(static_cast<uint16_t>(w.y & 0xFFFFu));
-  const float2 d = e4m3x2_to_f32x2(static_cast<uint16_t>(w.y >> 16));
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+// Four E4M3 codes (byte i of w = code i) -> two f16x2 words: lo holds codes 0
+// and 1, hi codes 2 and 3, the lower code in the lower half (exact: every
+// E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Two floats -> f16x2 (round to nearest even), `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// D (16 x 8, f32) += A (16 x 16, f16, row-major fragment) * B (16 x 8, f16,
+// column fragment): the warp-level tensor-core product.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Offset of V row t in a stage: 16 K rows, then the V rows in four groups of
+// 4 tokens, vgroup bytes apart.
+template <bool F8>
+__device__ __forceinline__ int v_row(int t, int row_bytes, int vgroup) {
+  return F8 ? kStepTokens * row_bytes + (t >> 2) * vgroup + (t & 3) * row_bytes : (kStepTokens + t) * row_bytes;
 }
 
 template <int D, int G, bool F8, bool SP>
@@ -81,10 +111,18 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = p.kv_heads;
   const int row_bytes = hkv * D * ESZ;               // one token, all kv heads
-  const int stage_bytes = 2 * kStepTokens * row_bytes;  // K then V
-  const int nstage = min(8, 196608 / stage_bytes);
-  float* pbuf = reinterpret_cast<float*>(smem + 196608);  // [hkv][16][G]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 196608 + 8 * kStepTokens * 8 * 4);
+  // A stage holds a step's 16 K rows as they lie in the cache (one bulk
+  // copy), then its V rows in four groups of 4 tokens, vgroup bytes apart.
+  // bf16: the groups are contiguous (one copy).  fp8: each group is its own
+  // copy and the groups are 32 bytes apart, so that the four lanes of a
+  // P V fragment group, which read the same dims of four tokens, read from
+  // four groups and so from four different banks.  (Padding every row
+  // instead needs 32 copies per step, which measured 1.6x slower.)
+  const int vgroup = F8 ? 4 * row_bytes + 32 : 4 * row_bytes;
+  const int stage_bytes = F8 ? kStepTokens * row_bytes + 4 * vgroup : 2 * kStepTokens * row_bytes;
+  const int nstage = min(8, kDecodeRing / stage_bytes);
+  float* pbuf = reinterpret_cast<float*>(smem + kDecodeRing);  // [hkv][16][G]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecodeRing + 8 * kStepTokens * 8 * 4);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 16);
   uint32_t* step_valid = reinterpret_cast<uint32_t*>(bars + 17);  // SP: valid-entry mask per stage
   const int warp = threadIdx.x >> 5;
@@ -171,7 +209,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         ok = false;
         break;
       }
-      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? kStepTokens * row_bytes : 0) + t * row_bytes;
+      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8>(t, row_bytes, vgroup) : t * row_bytes);
       if (t < nt && !valid) {  // zero-filled, so that P = 0 times it stays 0
         for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();  // before later bulk copies into these bytes
@@ -224,7 +262,14 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
           const uint32_t bytes = static_cast<uint32_t>(nt * row_bytes);
           mbar_arrive_expect_tx(full, 2 * bytes);
           bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
-          bulk_g2s(dst + kStepTokens * row_bytes, static_cast<const uint8_t*>(p.v_cache) + off, bytes, full);
+          const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
+          if (!F8) {
+            bulk_g2s(dst + kStepTokens * row_bytes, vsrc, bytes, full);
+          } else {
+            for (int g4 = 0; 4 * g4 < nt; ++g4)
+              bulk_g2s(dst + v_row<F8>(4 * g4, row_bytes, vgroup), vsrc + 4 * g4 * row_bytes,
+                       static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
+          }
         } else {
           mbar_arrive(full);  // invalid block: the step's rows are skipped
         }
@@ -238,6 +283,231 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
       if (!ok) {
         for (int i = 0; i < nstage; ++i)
           if (filled & (1u << i)) mbar_wait_for(smem_u32(&bars[i]), (fill_phase >> i) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp < hkv && F8) {
+    // ------------------------------------------ kv head `warp`, fp8 codes
+    // Both products run on the tensor cores (mma.sync m16n8k16, f16 operands,
+    // f32 accumulation).  Lane = 4 g + u: g is the fragment's group (a token
+    // row of S^T, a dim row of O^T, a head column of the B operands), u the
+    // thread in the group.
+    //   S^T[16 tokens x 8 heads] = K[16 x D] Q^T[D x 8]: k-step s, logical
+    //     k = 2u + b + 8c maps to dim u D/4 + 4s + 2c + b, so a thread's
+    //     codes of one token are D/4 consecutive bytes.
+    //   O^T[D x 8 heads] += V^T[D x 16 tokens] P^T[16 x 8]: tile i, row g
+    //     is dim g D/8 + 2i, row g + 8 is dim g D/8 + 2i + 1; logical
+    //     k = 2u + b + 8c maps to token 4u + b + 2c, so a thread reads D/8
+    //     consecutive codes of each token of V group u.
+    // Heads >= G are zero columns.  E4M3 codes widen exactly to f16; q is
+    // scaled by a power of two per head into f16's range (undone on the
+    // scores), P is in [0, 256].
+    const int h = warp;
+    const int gq = lane >> 2;
+    const int u = lane & 3;
+    constexpr int KS = D / 16;  // k-steps of S, tiles of O
+    uint32_t qb[KS][2];
+    float qscale;  // 2^-e of head gq
+    {
+      float qv[D / 4];
+      if (gq < G) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + gq) * D + u * (D / 4));
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 w = __ldg(src + c);
+          bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
+          bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
+          bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
+          bf16x2_to_f32(w.w, qv[8 * c + 6], qv[8 * c + 7]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) qv[i] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 4; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // 2^e puts the head's largest |q| in [2^14, 2^15): below f16's largest
+      // value, and every bf16 value of the head that is not negligible keeps
+      // its 8 significant bits.
+      const int e = amax > 0.f ? max(-60, min(60, 14 - ilogbf(amax))) : 0;
+      const float up = ldexpf(1.f, e);
+      qscale = ldexpf(1.f, -e);
+#pragma unroll
+      for (int s2 = 0; s2 < KS; ++s2) {
+        qb[s2][0] = pack_f16x2(qv[4 * s2] * up, qv[4 * s2 + 1] * up);
+        qb[s2][1] = pack_f16x2(qv[4 * s2 + 2] * up, qv[4 * s2 + 3] * up);
+      }
+    }
+    // This thread's S^T columns are heads 2u and 2u + 1.
+    const float sl = p.scale_log2 * __ldg(p.k_scale + h);
+    const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
+                          sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
+    const float vsc = __ldg(p.v_scale + h);
+    float m[2] = {-INFINITY, -INFINITY};
+    float lpart[2] = {0.f, 0.f};
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float* pw = pbuf + h * kStepTokens * 8;  // P of the step: [16 tokens][8 heads]
+    int slot = 0;
+    uint32_t phase = 0u;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      const int t0 = t_begin + s * kStepTokens;
+      const int nt = min(kStepTokens, t_end - t0);
+      ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint8_t* kst = smem + slot * stage_bytes;
+      const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
+      // ---- S^T = K Q^T (two accumulator chains)
+      // With D = 128 a thread reads 32 bytes of a row; odd groups read the
+      // upper 16 first, so that the two groups of a quarter warp, whose rows
+      // lie a multiple of 128 bytes apart, hit different banks.
+      uint32_t kw[2][D / 16];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint4* src = reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * row_bytes + h * D + u * (D / 4));
+        if (D == 128) {
+          const int sw = gq & 1;
+          const uint4 wa = src[sw];
+          const uint4 wb = src[sw ^ 1];
+          const uint4 w0 = sw ? wb : wa;
+          const uint4 w1 = sw ? wa : wb;
+          kw[rr][0] = w0.x;
+          kw[rr][1] = w0.y;
+          kw[rr][2] = w0.z;
+          kw[rr][3] = w0.w;
+          kw[rr][4 % (D / 16)] = w1.x;
+          kw[rr][5 % (D / 16)] = w1.y;
+          kw[rr][6 % (D / 16)] = w1.z;
+          kw[rr][7 % (D / 16)] = w1.w;
+        } else {
+          const uint4 w = src[0];
+          kw[rr][0] = w.x;
+          kw[rr][1] = w.y;
+          kw[rr][2] = w.z;
+          kw[rr][3] = w.w;
+        }
+      }
+      float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int s2 = 0; s2 < KS; ++s2) {
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(kw[0][s2], a0, a2);
+        e4m3x4_to_f16x2x2(kw[1][s2], a1, a3);
+        mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
+      }
+      // sc[rr][hh]: token gq + 8 rr, head 2u + hh
+      float sc[2][2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int t = gq + 8 * rr;
+        const bool tv = t < nt && ((vmask >> t) & 1u);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          sc[rr][hh] = (tv && 2 * u + hh < G) ? (sa[0][2 * rr + hh] + sa[1][2 * rr + hh]) * slh[hh] : -INFINITY;
+      }
+      // ---- online softmax per head (the 8 lanes of one u hold its 16 tokens)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float mx = fmaxf(sc[0][hh], sc[1][hh]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m[hh] + 8.0f || (m[hh] == -INFINITY && mx != -INFINITY)) {  // uniform over the 8 lanes
+          const float f = (m[hh] == -INFINITY) ? 0.f : ex2_approx(m[hh] - mx);
+          lpart[hh] *= f;
+#pragma unroll
+          for (int i = 0; i < KS; ++i) {
+            o[i][hh] *= f;
+            o[i][2 + hh] *= f;
+          }
+          m[hh] = mx;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const float pv = (m[hh] == -INFINITY) ? 0.f : ex2_approx(sc[rr][hh] - m[hh]);
+          lpart[hh] += pv;
+          pw[(gq + 8 * rr) * 8 + 2 * u + hh] = pv;
+        }
+      }
+      __syncwarp();
+      // ---- O^T += V^T P^T
+      const uint32_t pb0 = pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
+      const uint32_t pb1 = pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
+      uint32_t vw[4][D / 32];  // tokens 4u .. 4u + 3 (V group u): this thread's D/8 codes each
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int t = 4 * u + q4;
+        const uint8_t* src = kst + v_row<F8>(t, row_bytes, vgroup) + h * D + gq * (D / 8);
+        if (D == 128) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src);
+          vw[q4][0] = w.x;
+          vw[q4][1 % (D / 32)] = w.y;
+          vw[q4][2 % (D / 32)] = w.z;
+          vw[q4][3 % (D / 32)] = w.w;
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(src);
+          vw[q4][0] = w.x;
+          vw[q4][1 % (D / 32)] = w.y;
+        }
+        // rows past the range hold stale bytes: zero codes (P is 0 there)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) vw[q4][c] = t < nt ? vw[q4][c] : 0u;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
+        const uint32_t y = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(x, a0, a1);
+        e4m3x4_to_f16x2x2(y, a2, a3);
+        mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
+      if (++slot == nstage) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float l = lpart[hh];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int j = 2 * u + hh;
+        if (j >= G) continue;
+        const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
+        const float inv = empty ? 0.f : vsc / l;
+        const float lse_v = empty ? -INFINITY : m[hh] * kLn2d + logf(l);
+        const int hq = h * G + j;
+        // dims gq D/8 + 2i (o[i][hh]) and + 2i + 1 (o[i][2 + hh])
+        if (n_splits == 1) {
+          uint32_t pk[KS];
+#pragma unroll
+          for (int i = 0; i < KS; ++i) pk[i] = pack_bf16x2(o[i][hh] * inv, o[i][2 + hh] * inv);
+          uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + gq * (D / 8);
+#pragma unroll
+          for (int c = 0; c < KS / 4; ++c)
+            reinterpret_cast<uint4*>(dst)[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          if (p.lse && gq == 0) p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = lse_v;
+        } else {
+          float* dst = p.ws_o + (static_cast<int64_t>(item) * p.heads + hq) * D + gq * (D / 8);
+#pragma unroll
+          for (int c = 0; c < KS / 2; ++c)
+            reinterpret_cast<float4*>(dst)[c] = make_float4(o[2 * c][hh] * inv, o[2 * c][2 + hh] * inv,
+                                                            o[2 * c + 1][hh] * inv, o[2 * c + 1][2 + hh] * inv);
+          if (gq == 0) p.ws_lse[static_cast<int64_t>(item) * p.heads + hq] = lse_v;
+        }
       }
     }
   } else if (warp < hkv) {
@@ -259,8 +529,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         bf16x2_to_f32(w.w, qf[j][8 * c + 6], qf[j][8 * c + 7]);
       }
     }
-    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
-    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
+    const float sl = p.scale_log2;
     float m[G], lpart[G], o[G][OPL];
 #pragma unroll
     for (int j = 0; j < G; ++j) {
@@ -291,31 +560,21 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
         if (t < nt) {
-          const uint8_t* kb = kst + t * row_bytes + (h * D + r * DPL) * ESZ;
+          const uint8_t* kb = kst + t * row_bytes + (h * D + r * DPL) * 2;
 #pragma unroll
           for (int c = 0; c < DPL / 8; ++c) {
             float kf[8];
-            if (F8) {
-              e4m3x8_to_f32(reinterpret_cast<const uint2*>(kb)[c], kf);
-            } else {
-              const uint4 w = reinterpret_cast<const uint4*>(kb)[c];
-              bf16x2_to_f32(w.x, kf[0], kf[1]);
-              bf16x2_to_f32(w.y, kf[2], kf[3]);
-              bf16x2_to_f32(w.z, kf[4], kf[5]);
-              bf16x2_to_f32(w.w, kf[6], kf[7]);
-            }
+            const uint4 w = reinterpret_cast<const uint4*>(kb)[c];
+            bf16x2_to_f32(w.x, kf[0], kf[1]);
+            bf16x2_to_f32(w.y, kf[2], kf[3]);
+            bf16x2_to_f32(w.z, kf[4], kf[5]);
+            bf16x2_to_f32(w.w, kf[6], kf[7]);
 #pragma unroll
             for (int j = 0; j < G; ++j)
 #pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                if (F8) {  // scalar FMAs measure faster next to the E4M3 conversions
-                  acc[j].x = fmaf(qf[j][8 * c + e], kf[e], acc[j].x);
-                  acc[j].y = fmaf(qf[j][8 * c + e + 1], kf[e + 1], acc[j].y);
-                } else {
-                  acc[j] = ffma2(make_float2(qf[j][8 * c + e], qf[j][8 * c + e + 1]),
-                                 make_float2(kf[e], kf[e + 1]), acc[j]);
-                }
-              }
+              for (int e = 0; e < 8; e += 2)
+                acc[j] = ffma2(make_float2(qf[j][8 * c + e], qf[j][8 * c + e + 1]),
+                               make_float2(kf[e], kf[e + 1]), acc[j]);
           }
         }
 #pragma unroll
@@ -356,24 +615,9 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         float pv[G];
 #pragma unroll
         for (int j = 0; j < G; ++j) pv[j] = pw[t * G + j];
-        const uint8_t* vb = vst + t * row_bytes + (h * D + lane * OPL) * ESZ;
-        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vb);
+        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vst + t * row_bytes + (h * D + lane * OPL) * 2);
         float vf[OPL];
-        if (F8) {
-          if (OPL == 4) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(vb);
-            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w & 0xFFFFu));
-            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w >> 16));
-            vf[0] = a.x;
-            vf[1 % OPL] = a.y;
-            vf[2 % OPL] = b.x;
-            vf[3 % OPL] = b.y;
-          } else {
-            const float2 a = e4m3x2_to_f32x2(*vr);
-            vf[0] = a.x;
-            vf[1 % OPL] = a.y;
-          }
-        } else if (OPL == 4) {
+        if (OPL == 4) {
           const uint2 w = *reinterpret_cast<const uint2*>(vr);
           bf16x2_to_f32(w.x, vf[0], vf[1 % OPL]);
           bf16x2_to_f32(w.y, vf[2 % OPL], vf[3 % OPL]);
@@ -385,15 +629,10 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
         for (int j = 0; j < G; ++j)
 #pragma unroll
           for (int i = 0; i < OPL; i += 2) {
-            if (F8) {
-              o[j][i] = fmaf(pv[j], vf[i], o[j][i]);
-              o[j][i + 1] = fmaf(pv[j], vf[i + 1], o[j][i + 1]);
-            } else {
-              const float2 r = ffma2(make_float2(pv[j], pv[j]), make_float2(vf[i], vf[i + 1]),
-                                     make_float2(o[j][i], o[j][i + 1]));
-              o[j][i] = r.x;
-              o[j][i + 1] = r.y;
-            }
+            const float2 r = ffma2(make_float2(pv[j], pv[j]), make_float2(vf[i], vf[i + 1]),
+                                   make_float2(o[j][i], o[j][i + 1]));
+            o[j][i] = r.x;
+            o[j][i + 1] = r.y;
           }
       }
       __syncwarp();
@@ -410,7 +649,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
 #pragma unroll
         for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
         const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
-        const float inv = empty ? 0.f : vsc / l;
+        const float inv = empty ? 0.f : 1.f / l;
         const float lse_v = empty ? -INFINITY : m[j] * kLn2d + logf(l);
         const int hq = h * G + j;
         if (n_splits == 1) {
