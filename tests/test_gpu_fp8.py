@@ -244,7 +244,7 @@ def test_fp8_workspace_is_required():
 CTX = [1, 2, 15, 16, 17, 63, 64, 65, 1000, 1023, 1024, 1025, 2048, 3001]
 
 
-def _mixed(ctx, qlen, Hq, Hkv, d, seed):
+def _mixed(ctx, qlen, Hq, Hkv, d, seed, qmul=1.0):
     B = len(ctx)
     cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
     need = [(int(c) + 63) // 64 for c in ctx]
@@ -268,6 +268,8 @@ def _mixed(ctx, qlen, Hq, Hkv, d, seed):
         vpp.vpp_kv_append_fp8(ks_[b].to(DEV), vs_[b].to(DEV), kc, vc, ksd, vsd, 0,
                               block_table=torch.from_numpy(table[b].copy()).to(DEV))
     q = gen((int(cu[-1]), Hq, d), seed + 999, std)
+    if qmul != 1.0:
+        q = (q.float() * qmul).to(torch.bfloat16)
     lse = torch.empty((Hq, int(cu[-1])), dtype=torch.float32, device=DEV)
     out = vpp.vpp_mixed_attn_fp8(q.to(DEV), kc, vc, ksd, vsd, torch.from_numpy(table).to(DEV), cu,
                                  np.asarray(ctx, dtype=np.int32), lse=lse)
@@ -283,6 +285,13 @@ def _mixed(ctx, qlen, Hq, Hkv, d, seed):
 @pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (64, 8, 64), (4, 1, 64), (128, 8, 128)])
 def test_fp8_decode_rows_match_oracle(Hq, Hkv, d):
     _mixed(CTX, [1] * len(CTX), Hq, Hkv, d, seed=Hq + d)
+
+
+@pytest.mark.parametrize("qmul", [1e-6, 40.0])
+def test_fp8_decode_rows_with_extreme_query_scales(qmul):
+    # The tensor-core decode scales q by a power of two per head into f16's
+    # range: tiny and large queries must give the oracle's result.
+    _mixed([1, 17, 1000, 2048, 3001], [1] * 5, 32, 8, 128, seed=5, qmul=qmul)
 
 
 def test_fp8_mixed_prefill_and_decode():
