@@ -32,6 +32,12 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int* status = nullptr;
+  // Side stream for the decode rows of a mixed batch, so that they run beside
+  // the prefill segments, and its fork / join events.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr;
+  cudaEvent_t ev_join = nullptr;
+  std::mutex side_mutex;  // one fork ... join sequence at a time
 };
 
 std::mutex g_mutex;
@@ -64,6 +70,10 @@ int device_state(DeviceState** out) {
         return VPP_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
+    if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.ev_join, cudaEventDisableTiming) != cudaSuccess)
+      return VPP_ERR_CUDA;
     s.ready = true;
   }
   *out = &s;
@@ -399,51 +409,15 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
     return VPP_ERR_INVALID;
   }
 
-  static AttnParams zero_params;
-  AttnParams p = zero_params;
-  p.heads = heads;
-  p.kv_heads = kv_heads;
-  p.group = heads / kv_heads;
-  p.num_blocks = num_blocks;
-  p.paged = fp8 ? 0 : 1;
-  p.scale_log2 =
+  const float scale_log2 =
       (softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)head_dim_qk)) * 1.4426950408889634f;
-  p.block_table = block_table;
-  p.out = static_cast<uint16_t*>(out);
-  p.lse = lse;
-  p.lse_stride = total_q;
-  p.k_scale = fp8 ? k_scale : nullptr;
-  p.v_scale = fp8 ? v_scale : nullptr;
-  p.status = ds->status;
-  for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
-    const int cnt = std::min(kMaxAttnSegs, n - i0);
-    int64_t cta = 0;
-    p.n_segs = cnt;
-    for (int i = 0; i < cnt; ++i) {
-      const int b = order[i0 + i];
-      AttnSeg& s = p.segs[i];
-      s.q_start = cu_seqlens_q[b];
-      s.q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-      s.kv_len = ctx_lens[b];
-      s.table_off = b * max_blocks_per_seq;
-      s.n_pairs = pairs_for(s.q_len, p.group);
-      s.n_splits = 1;
-      s.split_keys = 0;
-      s.cta_begin = (int32_t)cta;
-      s.kv_base = fp8 ? (int32_t)kv_base[i0 + i] : 0;
-      s.ws_row0 = 0;
-      cta += (int64_t)s.n_pairs * kv_heads;
-    }
-    if (cta > INT32_MAX) return VPP_ERR_INVALID;
-    if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) != cudaSuccess)
-      return VPP_ERR_CUDA;
-  }
 
   // Decode rows, longest context first.
   static DecodeParams zero_dp;
   DecodeParams dp = zero_dp;
   int drows[kMaxBatch];
   int nd = 0;
+  int64_t dp_items = 0;
   for (int b = 0; b < batch; ++b)
     if (is_decode_row(cu_seqlens_q, b, heads, kv_heads, head_dim_qk, head_dim_v) && ctx_lens[b] > 0)
       drows[nd++] = b;
@@ -459,13 +433,14 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
       items += ceil_div(ctx_lens[b], kDecodeSplitTokens);
     }
     if (items > INT32_MAX) return VPP_ERR_INVALID;
+    dp_items = items;
     dp.n_rows = nd;
     dp.heads = heads;
     dp.kv_heads = kv_heads;
     dp.split_tokens = kDecodeSplitTokens;
     dp.num_blocks = num_blocks;
     dp.max_blocks_per_seq = max_blocks_per_seq;
-    dp.scale_log2 = p.scale_log2;
+    dp.scale_log2 = scale_log2;
     dp.q = static_cast<const uint16_t*>(q);
     dp.k_cache = k_cache;
     dp.v_cache = v_cache;
@@ -481,10 +456,77 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
                                            round_up((size_t)items * heads * head_dim_v * 4, 256));
     }
     dp.status = ds->status;
-    if (launch_decode(dp, (int)items, head_dim_qk, fp8, false, ds->num_sms, st) != cudaSuccess)
-      return VPP_ERR_CUDA;
   }
-  return VPP_OK;
+
+  // The decode rows (HBM-bound) are launched first, on the side stream, and
+  // the prefill segments (tensor-bound) on the caller's stream: the two
+  // kernels' CTAs share the SMs instead of running one after the other.
+  // They write disjoint rows of out / lse and disjoint workspace.  (Measured
+  // on the 256-row mixed batch: -1% on a bf16 cache, -5% on an fp8 one; a
+  // highest-priority side stream gained nothing.)
+  std::unique_lock<std::mutex> side_lock(ds->side_mutex, std::defer_lock);
+  cudaStream_t dst = st;
+  const bool fork = nd > 0 && n > 0;
+  if (fork) {
+    side_lock.lock();
+    if (cudaEventRecord(ds->ev_fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(ds->side, ds->ev_fork, 0) != cudaSuccess)
+      return VPP_ERR_CUDA;
+    dst = ds->side;
+  }
+  int err = VPP_OK;
+  if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms, dst) != cudaSuccess)
+    err = VPP_ERR_CUDA;
+  if (fork && cudaEventRecord(ds->ev_join, ds->side) != cudaSuccess) err = VPP_ERR_CUDA;
+  if (err == VPP_OK) {
+    static AttnParams zero_params;
+    AttnParams p = zero_params;
+    p.heads = heads;
+    p.kv_heads = kv_heads;
+    p.group = heads / kv_heads;
+    p.num_blocks = num_blocks;
+    p.paged = fp8 ? 0 : 1;
+    p.scale_log2 = scale_log2;
+    p.block_table = block_table;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.lse_stride = total_q;
+    p.k_scale = fp8 ? k_scale : nullptr;
+    p.v_scale = fp8 ? v_scale : nullptr;
+    p.status = ds->status;
+    for (int i0 = 0; i0 < n; i0 += kMaxAttnSegs) {
+      const int cnt = std::min(kMaxAttnSegs, n - i0);
+      int64_t cta = 0;
+      p.n_segs = cnt;
+      for (int i = 0; i < cnt; ++i) {
+        const int b = order[i0 + i];
+        AttnSeg& s = p.segs[i];
+        s.q_start = cu_seqlens_q[b];
+        s.q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        s.kv_len = ctx_lens[b];
+        s.table_off = b * max_blocks_per_seq;
+        s.n_pairs = pairs_for(s.q_len, p.group);
+        s.n_splits = 1;
+        s.split_keys = 0;
+        s.cta_begin = (int32_t)cta;
+        s.kv_base = fp8 ? (int32_t)kv_base[i0 + i] : 0;
+        s.ws_row0 = 0;
+        cta += (int64_t)s.n_pairs * kv_heads;
+      }
+      if (cta > INT32_MAX) {
+        err = VPP_ERR_INVALID;
+        break;
+      }
+      if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) != cudaSuccess) {
+        err = VPP_ERR_CUDA;
+        break;
+      }
+    }
+  }
+  // Join even after an error, so that the caller's stream covers every
+  // launch that was made.
+  if (fork && cudaStreamWaitEvent(st, ds->ev_join, 0) != cudaSuccess && err == VPP_OK) err = VPP_ERR_CUDA;
+  return err;
 }
 
 // Top-k sparse prefix attention (DSA-style) of one chunk through the decode
