@@ -105,7 +105,9 @@ struct BatchPos {
   }
 };
 
-// One grid-stride loop over (new row, 16-element vector) of one tensor.
+// One grid-stride loop over (new row, 16-element vector) of one tensor, two
+// vectors per thread and iteration (both loads issued before either store),
+// with the (row, vector) index advanced by the stride instead of divided.
 template <typename Pos>
 __device__ __forceinline__ void quantise_rows(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                               const float* __restrict__ scale, int64_t tokens, int d,
@@ -113,16 +115,51 @@ __device__ __forceinline__ void quantise_rows(const uint4* __restrict__ src, uin
   const int64_t total = tokens * vec_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int vec_per_head = d / 16;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t t = i / vec_per_row;
-    const int v = static_cast<int>(i - t * vec_per_row);
-    int64_t row;
-    if (!pos.slot(t, num_blocks, &row)) {
-      if (v == 0) record_status(status, kStatusInvalid);
-      continue;
+  const int64_t dt = stride / vec_per_row;
+  const int dv = static_cast<int>(stride - dt * vec_per_row);
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t t = i / vec_per_row;
+  int v = static_cast<int>(i - t * vec_per_row);
+  auto advance = [&](int64_t& tt, int& vv) {
+    tt += dt;
+    vv += dv;
+    if (vv >= vec_per_row) {
+      vv -= vec_per_row;
+      ++tt;
     }
-    const float s = __ldg(scale + v / vec_per_head);
-    dst[row * vec_per_row + v] = quantise16(__ldg(&src[2 * i]), __ldg(&src[2 * i + 1]), s, __frcp_rn(s));
+  };
+  for (; i < total; i += 2 * stride) {
+    int64_t t2 = t;
+    int v2 = v;
+    advance(t2, v2);
+    const bool has2 = i + stride < total;
+    int64_t row = 0, row2 = 0;
+    const bool ok1 = pos.slot(t, num_blocks, &row);
+    const bool ok2 = has2 && pos.slot(t2, num_blocks, &row2);
+    uint4 a1 = make_uint4(0u, 0u, 0u, 0u), b1 = a1, a2 = a1, b2 = a1;
+    if (ok1) {
+      a1 = __ldg(&src[2 * i]);
+      b1 = __ldg(&src[2 * i + 1]);
+    }
+    if (ok2) {
+      a2 = __ldg(&src[2 * (i + stride)]);
+      b2 = __ldg(&src[2 * (i + stride) + 1]);
+    }
+    if (ok1) {
+      const float sc = __ldg(scale + v / vec_per_head);
+      dst[row * vec_per_row + v] = quantise16(a1, b1, sc, __frcp_rn(sc));
+    } else if (v == 0) {
+      record_status(status, kStatusInvalid);
+    }
+    if (ok2) {
+      const float sc = __ldg(scale + v2 / vec_per_head);
+      dst[row2 * vec_per_row + v2] = quantise16(a2, b2, sc, __frcp_rn(sc));
+    } else if (has2 && v2 == 0) {
+      record_status(status, kStatusInvalid);
+    }
+    t = t2;
+    v = v2;
+    advance(t, v);
   }
 }
 
