@@ -308,6 +308,54 @@ def test_mixed_batch_small():
     assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
 
 
+def test_mixed_batch_replays_in_a_cuda_graph():
+    # The decode rows run on a side stream forked from the caller's stream by
+    # events; a graph captured from the caller's stream must hold both branches
+    # and replay to the eager result bit for bit.
+    Hq, Hkv, d, nb = 8, 2, 128, 120
+    ctx = np.array([500, 1, 1700, 300, 64], dtype=np.int32)
+    qlen = np.array([200, 1, 1, 100, 1], dtype=np.int32)
+    B = len(ctx)
+    cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    maxb = int(max((c + 63) // 64 for c in ctx))
+    perm = np.random.default_rng(21).permutation(nb).astype(np.int32)
+    table = np.full((B, maxb), -1, dtype=np.int32)
+    kc = torch.zeros((nb, 64, Hkv, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    off = 0
+    for b in range(B):
+        n = (ctx[b] + 63) // 64
+        table[b, :n] = perm[off:off + n]
+        off += n
+        k = gen((int(ctx[b]), Hkv, d), 400 + b, 1 / math.sqrt(d))
+        v = gen((int(ctx[b]), Hkv, d), 500 + b, 1 / math.sqrt(d))
+        vpp.vpp_kv_append(k.to(DEV), v.to(DEV), kc, vc, 0, block_table=torch.from_numpy(table[b].copy()).to(DEV))
+    q = gen((int(cu[-1]), Hq, d), 600, 1 / math.sqrt(d)).to(DEV)
+    tab = torch.from_numpy(table).to(DEV)
+    need = vpp.mixed_attn_workspace_size(cu, ctx, Hq, Hkv, d, d)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=DEV)
+    out_e = torch.empty((int(cu[-1]), Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse_e = torch.empty((Hq, int(cu[-1])), dtype=torch.float32, device=DEV)
+    vpp.vpp_mixed_attn(q, kc, vc, tab, cu, ctx, out=out_e, lse=lse_e, workspace=ws)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    out_g = torch.full_like(out_e, float("nan"))
+    lse_g = torch.full_like(lse_e, float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device=DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            vpp.vpp_mixed_attn(q, kc, vc, tab, cu, ctx, out=out_g, lse=lse_g, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16))
+    assert torch.equal(lse_g, lse_e)
+
+
 def test_empty_chunk_is_a_noop():
     q = torch.empty((0, 8, 128), dtype=torch.bfloat16, device=DEV)
     kc = torch.zeros((64, 2, 128), dtype=torch.bfloat16, device=DEV)
