@@ -462,10 +462,14 @@ def measure_topk(dev, stream, hbm, peak_tf):
     table = torch.from_numpy(W.block_table(nb, nb + 8, w.seed + 99)).to(dev)
     kc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
     vc = torch.zeros_like(kc)
+    kc8 = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.uint8, device=dev)
+    vc8 = torch.zeros_like(kc8)
+    s8 = torch.full((w.kv_heads,), 0.5 / 448.0, dtype=torch.float32, device=dev)  # |k|, |v| < 0.5 here
     qs = []
     for ci, (p0, c0) in enumerate(chunks):
         qi, ki, vi = W.chunk_tensors(w, ci, dev)
         vpp.vpp_kv_append(ki, vi, kc, vc, p0, block_table=table)
+        vpp.vpp_kv_append_fp8(ki, vi, kc8, vc8, s8, s8, p0, block_table=table)
         qs.append(qi)
         del ki, vi
     out = torch.empty((w.chunk, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
@@ -476,6 +480,9 @@ def measure_topk(dev, stream, hbm, peak_tf):
         idx, lens = W.topk_indices(P, C, W.TOPK, ci, device=dev)
         ts = time_events(lambda: vpp.vpp_topk_chunk_attn(qs[ci], kc, vc, P, idx, lens, block_table=table,
                                                          out=out[:C], workspace=ws_t), 5, stream)
+        ts8 = time_events(lambda: vpp.vpp_topk_chunk_attn_fp8(qs[ci], kc8, vc8, s8, s8, P, idx, lens,
+                                                              block_table=table, out=out[:C], workspace=ws_t),
+                          5, stream)
         td = time_events(lambda: vpp.vpp_chunk_attn_ex(qs[ci], kc, vc, P, block_table=table, out=out[:C],
                                                        num_splits=1), 3, stream)
         n_listed = int(lens.to(torch.int64).sum())
@@ -487,6 +494,7 @@ def measure_topk(dev, stream, hbm, peak_tf):
         rows.append({"k": ci, "prefix": P, "sparse_ms": round(ts, 3), "dense_ms": round(td, 3),
                      "gathered_gb": round(byts / 1e9, 2), "sparse_gbs": round(byts / (ts / 1e3) / 1e9, 1),
                      "sparse_frac_hbm": round(byts / (ts / 1e3) / 1e9 / hbm, 4),
+                     "sparse_fp8_ms": round(ts8, 3), "sparse_fp8_gbs": round(byts / 2 / (ts8 / 1e3) / 1e9, 1),
                      "sparse_tflops": round(fl / (ts / 1e3) / 1e12, 1),
                      "dense_tflops": round(dfl / (td / 1e3) / 1e12, 1)})
     return {"workload": f"dsa128k: 32/8 heads, d 128, 8 chunks of 16384, {W.TOPK} listed keys per query token",
