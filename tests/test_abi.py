@@ -70,6 +70,14 @@ def test_host_validation_rejects_bad_arguments(lib):
     ctx = (ctypes.c_int32 * 2)(4, 10)
     assert lib.vpp_mixed_attn(fake, fake, fake, fake, 4, 16, cu, ctx, 2, 8, 2, 128, 128, 0.0, fake, null,
                               null, 0, null) == vpp.VPP_ERR_INVALID
+    # at most 1024 sequences per mixed batch (the plan travels by value)
+    n = 1025
+    cu_big = (ctypes.c_int32 * (n + 1))(*range(n + 1))
+    ctx_big = (ctypes.c_int32 * n)(*([1] * n))
+    assert lib.vpp_mixed_attn(fake, fake, fake, fake, 4, 16, cu_big, ctx_big, n, 8, 2, 128, 128, 0.0, fake, null,
+                              null, 0, null) == vpp.VPP_ERR_INVALID
+    assert lib.vpp_kv_append_varlen(fake, fake, fake, fake, fake, 4, 16, cu_big, ctx_big, n, 2, 128, 128,
+                                    null) == vpp.VPP_ERR_INVALID
     assert lib.vpp_selftest_wait_timeout(0, null) == vpp.VPP_ERR_INVALID
     # fp8 cache: scales are required and 4-byte aligned
     assert lib.vpp_kv_append_fp8(fake, fake, fake, fake, null, fake, fake, 2, 0, 29, 2, 128, 128,

@@ -308,6 +308,48 @@ def test_mixed_batch_small():
     assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
 
 
+def test_mixed_batch_at_the_sequence_limit():
+    # 1024 sequences (the plan's limit): 80 prefill segments, more than one
+    # chunk-kernel launch holds (64), and 944 decode rows of the split-KV kernel.
+    Hq, Hkv, d = 8, 2, 64
+    rng = np.random.default_rng(31)
+    B, n_pre = 1024, 80
+    qlen = np.ones(B, dtype=np.int32)
+    qlen[:n_pre] = rng.integers(2, 41, n_pre)
+    ctx = (qlen + rng.integers(0, 160, B)).astype(np.int32)
+    order = rng.permutation(B)  # prefill segments and decode rows interleaved
+    qlen, ctx = qlen[order], ctx[order]
+    cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    need = [(int(c) + 63) // 64 for c in ctx]
+    maxb, nb = max(need), sum(need) + 4
+    perm = rng.permutation(nb).astype(np.int32)
+    table = np.full((B, maxb), -1, dtype=np.int32)
+    off = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[off:off + need[b]]
+        off += need[b]
+    std = 1 / math.sqrt(d)
+    k_all = gen((int(ctx.sum()), Hkv, d), 700, std)
+    v_all = gen((int(ctx.sum()), Hkv, d), 701, std)
+    starts = np.concatenate([[0], np.cumsum(ctx)])
+    # the whole cache through one varlen append (every token of every sequence is new)
+    kc = torch.full((nb, 64, Hkv, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vc = torch.full_like(kc, float("nan"))
+    tab = torch.from_numpy(table).to(DEV)
+    cu_all = starts.astype(np.int32)
+    vpp.vpp_kv_append_varlen(k_all.to(DEV), v_all.to(DEV), kc, vc, tab, cu_all, ctx)
+    q = gen((int(cu[-1]), Hq, d), 702, std)
+    lse = torch.empty((Hq, int(cu[-1])), dtype=torch.float32, device=DEV)
+    out = vpp.vpp_mixed_attn(q.to(DEV), kc, vc, tab, cu, ctx, lse=lse)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    ks = [to_np64(k_all[starts[b]:starts[b + 1]]) for b in range(B)]
+    vs = [to_np64(v_all[starts[b]:starts[b + 1]]) for b in range(B)]
+    ref, ref_lse = oracle.mixed_batch_attention(to_np64(q), ks, vs, cu, ctx)
+    assert_close(to_np64(out), ref)
+    assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
+
+
 def test_mixed_batch_replays_in_a_cuda_graph():
     # The decode rows run on a side stream forked from the caller's stream by
     # events; a graph captured from the caller's stream must hold both branches
