@@ -11,36 +11,40 @@
 //
 // Work item = (row, key range of split_tokens keys).  One CTA per item:
 //   warp Hkv (last)   producer: for every 16-token step, one 1-D bulk copy of
-//                     the step's K rows and one of its V rows (16 tokens x all
-//                     kv heads are contiguous inside a 64-token block), into a
-//                     ring of shared-memory stages with full/empty mbarriers.
-//   warps 0..Hkv-1    warp h serves kv head h and its G query heads.  Scores:
-//                     8 lanes per token (D/8 dims each, 4 tokens per pass),
-//                     summed with three xor-shuffles.  Online softmax per head
+//                     the step's K rows and four of its V rows (16 tokens x
+//                     all kv heads are contiguous inside a 64-token block),
+//                     into a ring of shared-memory stages with full/empty
+//                     mbarriers.  The V rows go in four groups of 4 tokens
+//                     placed 32 (fp8) or 64 (bf16) bytes apart, so that the
+//                     fragment loads below spread over the banks.
+//   warps 0..Hkv-1    warp h serves kv head h and its G <= 8 query heads, on
+//                     the tensor cores (warp-level mma.sync m16n8k16, f32
+//                     accumulation): S^T = K Q^T, an online softmax per head
 //                     (running max and denominator, rescale only when the max
-//                     grows by more than 2^8).  P V: each lane owns D/32
-//                     output dims of every head; p is passed through shared
-//                     memory.
+//                     grows by more than 2^8), O^T += V^T P^T.  The CUDA cores
+//                     keep the softmax and the fragment shuffles; the G
+//                     multiply-adds per cached element leave them.
 // A range's result is final when the row has one range; otherwise the float32
 // partial output and its LSE go to the workspace and decode_merge combines
 // them ("02 · 并行策略与 PP 切分" note, §7).  HBM-bound: the algorithmic bytes
-// are ctx x Hkv x (dq + dv) x 2 per row plus q, out and the partials.
+// are ctx x Hkv x (dq + dv) x element bytes per row plus q, out and the
+// partials.
 //
-// fp8 cache (F8): the stages hold E4M3 codes, and both products run on the
-// tensor cores (warp-level mma.sync, f16 operands: every
-// E4M3 value is an f16 value; f32 accumulation), which takes the per-element
-// widening and the G multiply-adds per key off the CUDA cores.  kv head h's
-// k_scale joins its score scale and its v_scale multiplies the output, so
-// the cache bytes per row halve.
+// bf16 cache: bf16 operands, read from the stages as they are.  fp8 cache
+// (F8): the stages hold E4M3 codes, widened exactly to f16 operands (every
+// E4M3 value is an f16 value); q is scaled per head by a power of two into
+// f16's range.  kv head h's k_scale joins its score scale and its v_scale
+// multiplies the output, so the cache bytes per row halve.
 //
 // Top-k mode (SP): the rows are the query tokens of one prefill chunk and each
 // attends only the key positions its index row lists (DSA-style sparse
 // attention: VPP technical review §7; "02 · 并行策略与 PP 切分" §5.1).  A work
-// item is (token, range of 1024 list entries).  The producer warp gathers a
-// step's 16 listed keys with one bulk copy per key for K and one for V (all kv
-// heads of a key are contiguous); entries outside 0 .. position, or in a block
-// outside the pool, are zero-filled, masked out of the softmax and reported as
-// VPP_ERR_INVALID.
+// item is (token, range of 1024 list entries).  bf16: the producer warp
+// gathers a step's 16 listed keys with one bulk copy per key for K and one for
+// V (all kv heads of a key are contiguous).  fp8: each kv-head warp gathers its
+// own slices with 16-byte copies (sp_issue).  Entries outside 0 .. position,
+// or in a block outside the pool, are zero-filled, masked out of the softmax
+// and reported as VPP_ERR_INVALID.
 #include <algorithm>
 
 #include "common.cuh"
@@ -106,8 +110,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// D (16 x 8, f32) += A (16 x 16, f16, row-major fragment) * B (16 x 8, f16,
-// column fragment): the warp-level tensor-core product.
+// D (16 x 8, f32) += A (16 x 16, row-major fragment) * B (16 x 8, column
+// fragment), f16 or bf16 operands: the warp-level tensor-core product.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -120,13 +131,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // 4 tokens, vgroup bytes apart.
 template <bool F8>
 __device__ __forceinline__ int v_row(int t, int row_bytes, int vgroup) {
-  return F8 ? kStepTokens * row_bytes + (t >> 2) * vgroup + (t & 3) * row_bytes : (kStepTokens + t) * row_bytes;
+  return kStepTokens * row_bytes + (t >> 2) * vgroup + (t & 3) * row_bytes;
 }
 
 template <int D, int G, bool F8, bool SP>
 __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int DPL = D / 8;     // score dims per lane (8 lanes per token)
-  constexpr int OPL = D / 32;    // output dims per lane
   constexpr int ESZ = F8 ? 1 : 2;  // cache bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = p.kv_heads;
@@ -138,8 +147,8 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
   // P V fragment group, which read the same dims of four tokens, read from
   // four groups and so from four different banks.  (Padding every row
   // instead needs 32 copies per step, which measured 1.6x slower.)
-  const int vgroup = F8 ? 4 * row_bytes + 32 : 4 * row_bytes;
-  const int stage_bytes = F8 ? kStepTokens * row_bytes + 4 * vgroup : 2 * kStepTokens * row_bytes;
+  const int vgroup = 4 * row_bytes + (F8 ? 32 : 64);
+  const int stage_bytes = kStepTokens * row_bytes + 4 * vgroup;
   const int nstage = min(8, kDecodeRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kDecodeRing);  // [hkv][16][G]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecodeRing + 8 * kStepTokens * 8 * 4);
@@ -336,13 +345,9 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
           mbar_arrive_expect_tx(full, 2 * bytes);
           bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
           const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
-          if (!F8) {
-            bulk_g2s(dst + kStepTokens * row_bytes, vsrc, bytes, full);
-          } else {
-            for (int g4 = 0; 4 * g4 < nt; ++g4)
-              bulk_g2s(dst + v_row<F8>(4 * g4, row_bytes, vgroup), vsrc + 4 * g4 * row_bytes,
-                       static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
-          }
+          for (int g4 = 0; 4 * g4 < nt; ++g4)
+            bulk_g2s(dst + v_row<F8>(4 * g4, row_bytes, vgroup), vsrc + 4 * g4 * row_bytes,
+                     static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
         } else {
           mbar_arrive(full);  // invalid block: the step's rows are skipped
         }
@@ -358,8 +363,8 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
           if (filled & (1u << i)) mbar_wait_for(smem_u32(&bars[i]), (fill_phase >> i) & 1u, 100000000ull);
       }
     }
-  } else if (warp < hkv && F8) {
-    // ------------------------------------------ kv head `warp`, fp8 codes
+  } else if (warp < hkv) {
+    // ------------------------------------------------------ kv head `warp`
     // Both products run on the tensor cores (mma.sync m16n8k16, f16 operands,
     // f32 accumulation).  Lane = 4 g + u: g is the fragment's group (a token
     // row of S^T, a dim row of O^T, a head column of the B operands), u the
@@ -379,23 +384,35 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
     const int u = lane & 3;
     constexpr int KS = D / 16;  // k-steps of S, tiles of O
     uint32_t qb[KS][2];
-    float qscale;  // 2^-e of head gq
-    {
+    float qscale = 1.f;  // fp8: 2^-e of head gq
+    const uint4* qsrc = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D + u * (D / 4));
+    if (!F8) {
+      // bf16 operands: q's pairs are the B fragment as they are.
+      uint32_t qw[D / 8];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * c] = w.x;
+        qw[4 * c + 1] = w.y;
+        qw[4 * c + 2] = w.z;
+        qw[4 * c + 3] = w.w;
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < KS; ++s2) {
+        qb[s2][0] = qw[2 * s2];
+        qb[s2][1] = qw[2 * s2 + 1];
+      }
+    } else {
+      // f16 operands: q scaled per head by a power of two into f16's range.
       float qv[D / 4];
-      if (gq < G) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + gq) * D + u * (D / 4));
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint4 w = __ldg(src + c);
-          bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
-          bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
-          bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
-          bf16x2_to_f32(w.w, qv[8 * c + 6], qv[8 * c + 7]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i) qv[i] = 0.f;
+      for (int c = 0; c < D / 32; ++c) {
+        const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+        bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
+        bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
+        bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
+        bf16x2_to_f32(w.w, qv[8 * c + 6], qv[8 * c + 7]);
       }
       float amax = 0.f;
 #pragma unroll
@@ -415,10 +432,10 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
       }
     }
     // This thread's S^T columns are heads 2u and 2u + 1.
-    const float sl = p.scale_log2 * __ldg(p.k_scale + h);
+    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
     const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
                           sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
-    const float vsc = __ldg(p.v_scale + h);
+    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
     float m[2] = {-INFINITY, -INFINITY};
     float lpart[2] = {0.f, 0.f};
     float o[KS][4];
@@ -463,42 +480,58 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
       const uint8_t* kst = smem + slot * stage_bytes;
       const uint32_t vmask = warp_gather ? __shfl_sync(0xffffffffu, my_vm, slot) : (SP ? step_valid[slot] : 0xFFFFu);
       // ---- S^T = K Q^T (two accumulator chains)
-      // With D = 128 a thread reads 32 bytes of a row; odd groups read the
-      // upper 16 first, so that the two groups of a quarter warp, whose rows
-      // lie a multiple of 128 bytes apart, hit different banks.
-      uint32_t kw[2][D / 16];
+      // A thread reads KW words (D/4 elements) of each of its two token rows.
+      // Rows lie a multiple of 128 bytes apart, so a quarter warp's two
+      // groups would hit the same banks: the 16-byte pieces are read in an
+      // order that depends on the lane (and put back in place by selects).
+      constexpr int KW = D * ESZ / 16;  // 32-bit words of a thread's part of one K row
+      uint32_t kw[2][KW];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const uint4* src = reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * row_bytes + h * D + u * (D / 4));
-        if (D == 128) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * row_bytes + (h * D + u * (D / 4)) * ESZ);
+        uint4 w[KW / 4];
+        if (KW / 4 == 4) {
+          const int r = (u >> 1) | ((gq & 1) << 1);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = src[c ^ r];
+          // w[c] holds piece c ^ r: two conditional swaps put piece j in w[j]
+          if (r & 1) {
+            const uint4 t0 = w[0], t2 = w[2];
+            w[0] = w[1]; w[1] = t0; w[2] = w[3]; w[3] = t2;
+          }
+          if (r & 2) {
+            const uint4 t0 = w[0], t1 = w[1];
+            w[0] = w[2]; w[1] = w[3]; w[2] = t0; w[3] = t1;
+          }
+        } else if (KW / 4 == 2) {
           const int sw = gq & 1;
-          const uint4 wa = src[sw];
-          const uint4 wb = src[sw ^ 1];
-          const uint4 w0 = sw ? wb : wa;
-          const uint4 w1 = sw ? wa : wb;
-          kw[rr][0] = w0.x;
-          kw[rr][1] = w0.y;
-          kw[rr][2] = w0.z;
-          kw[rr][3] = w0.w;
-          kw[rr][4 % (D / 16)] = w1.x;
-          kw[rr][5 % (D / 16)] = w1.y;
-          kw[rr][6 % (D / 16)] = w1.z;
-          kw[rr][7 % (D / 16)] = w1.w;
+          const uint4 wa = src[sw], wb = src[sw ^ 1];
+          w[0] = sw ? wb : wa;
+          w[1 % (KW / 4)] = sw ? wa : wb;
         } else {
-          const uint4 w = src[0];
-          kw[rr][0] = w.x;
-          kw[rr][1] = w.y;
-          kw[rr][2] = w.z;
-          kw[rr][3] = w.w;
+          w[0] = src[0];
+        }
+#pragma unroll
+        for (int c = 0; c < KW / 4; ++c) {
+          kw[rr][4 * c] = w[c].x;
+          kw[rr][4 * c + 1] = w[c].y;
+          kw[rr][4 * c + 2] = w[c].z;
+          kw[rr][4 * c + 3] = w[c].w;
         }
       }
       float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int s2 = 0; s2 < KS; ++s2) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(kw[0][s2], a0, a2);
-        e4m3x4_to_f16x2x2(kw[1][s2], a1, a3);
-        mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
+        if (F8) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(kw[0][s2 % KW], a0, a2);
+          e4m3x4_to_f16x2x2(kw[1][s2 % KW], a1, a3);
+          mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
+        } else {
+          mma_16816_bf16(sa[s2 & 1], kw[0][(2 * s2) % KW], kw[1][(2 * s2) % KW], kw[0][(2 * s2 + 1) % KW],
+                         kw[1][(2 * s2 + 1) % KW], qb[s2][0], qb[s2][1]);
+        }
       }
       // sc[rr][hh]: token gq + 8 rr, head 2u + hh
       float sc[2][2];
@@ -536,38 +569,57 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
       }
       __syncwarp();
       // ---- O^T += V^T P^T
-      const uint32_t pb0 = pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
-      const uint32_t pb1 = pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
-      uint32_t vw[4][D / 32];  // tokens 4u .. 4u + 3 (V group u): this thread's D/8 codes each
+      const uint32_t pb0 = F8 ? pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq])
+                              : pack_bf16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
+      const uint32_t pb1 = F8 ? pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq])
+                              : pack_bf16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
+      // tokens 4u .. 4u + 3 (V group u): this thread's D/8 elements of each
+      constexpr int VW = D * ESZ / 32;  // 32-bit words of them
+      uint32_t vw[4][VW];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int t = 4 * u + q4;
-        const uint8_t* src = kst + v_row<F8>(t, row_bytes, vgroup) + h * D + gq * (D / 8);
-        if (D == 128) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src);
-          vw[q4][0] = w.x;
-          vw[q4][1 % (D / 32)] = w.y;
-          vw[q4][2 % (D / 32)] = w.z;
-          vw[q4][3 % (D / 32)] = w.w;
+        const uint8_t* src = kst + v_row<F8>(t, row_bytes, vgroup) + (h * D + gq * (D / 8)) * ESZ;
+        uint32_t w[VW];
+        if (VW == 8) {
+          // 32 bytes: the two 16-byte pieces in a lane-dependent order (bank
+          // spread across the groups 64 bytes apart), swapped back
+          const int sw = u >> 1;
+          const uint4 wa = reinterpret_cast<const uint4*>(src)[sw];
+          const uint4 wb = reinterpret_cast<const uint4*>(src)[sw ^ 1];
+          const uint4 w0 = sw ? wb : wa, w1 = sw ? wa : wb;
+          w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+          w[4 % VW] = w1.x; w[5 % VW] = w1.y; w[6 % VW] = w1.z; w[7 % VW] = w1.w;
+        } else if (VW == 4) {
+          const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+          w[0] = w0.x; w[1 % VW] = w0.y; w[2 % VW] = w0.z; w[3 % VW] = w0.w;
         } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(src);
-          vw[q4][0] = w.x;
-          vw[q4][1 % (D / 32)] = w.y;
+          const uint2 w0 = *reinterpret_cast<const uint2*>(src);
+          w[0] = w0.x; w[1 % VW] = w0.y;
         }
-        // rows past the range hold stale bytes: zero codes (P is 0 there)
+        // rows past the range hold stale bytes: zeros (P is 0 there)
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) vw[q4][c] = t < nt ? vw[q4][c] : 0u;
+        for (int c = 0; c < VW; ++c) vw[q4][c] = t < nt ? w[c] : 0u;
       }
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < KS; ++i) {
-        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-        const uint32_t x = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
-        const uint32_t y = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
         uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(x, a0, a1);
-        e4m3x4_to_f16x2x2(y, a2, a3);
-        mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+        if (F8) {
+          const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+          const uint32_t x = __byte_perm(vw[0][(i >> 1) % VW], vw[1][(i >> 1) % VW], sel);
+          const uint32_t y = __byte_perm(vw[2][(i >> 1) % VW], vw[3][(i >> 1) % VW], sel);
+          e4m3x4_to_f16x2x2(x, a0, a1);
+          e4m3x4_to_f16x2x2(y, a2, a3);
+          mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+        } else {
+          // word i of a token holds dims 2i, 2i + 1 of the thread's part
+          a0 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x5410u);
+          a1 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x7632u);
+          a2 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x5410u);
+          a3 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x7632u);
+          mma_16816_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
+        }
       }
       __syncwarp();
       if (!warp_gather && lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
@@ -606,165 +658,6 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
             reinterpret_cast<float4*>(dst)[c] = make_float4(o[2 * c][hh] * inv, o[2 * c][2 + hh] * inv,
                                                             o[2 * c + 1][hh] * inv, o[2 * c + 1][2 + hh] * inv);
           if (gq == 0) p.ws_lse[static_cast<int64_t>(item) * p.heads + hq] = lse_v;
-        }
-      }
-    }
-  } else if (warp < hkv) {
-    // ------------------------------------------------------ kv head `warp`
-    const int h = warp;
-    const int tt = lane >> 3;  // token within a pass of 4
-    const int r = lane & 7;    // dim group
-    const uint16_t* qrow = p.q + static_cast<int64_t>(row.q_row) * p.heads * D;
-    float qf[G][DPL];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + (h * G + j) * D + r * DPL);
-#pragma unroll
-      for (int c = 0; c < DPL / 8; ++c) {
-        const uint4 w = __ldg(src + c);
-        bf16x2_to_f32(w.x, qf[j][8 * c + 0], qf[j][8 * c + 1]);
-        bf16x2_to_f32(w.y, qf[j][8 * c + 2], qf[j][8 * c + 3]);
-        bf16x2_to_f32(w.z, qf[j][8 * c + 4], qf[j][8 * c + 5]);
-        bf16x2_to_f32(w.w, qf[j][8 * c + 6], qf[j][8 * c + 7]);
-      }
-    }
-    const float sl = p.scale_log2;
-    float m[G], lpart[G], o[G][OPL];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      m[j] = -INFINITY;
-      lpart[j] = 0.f;
-#pragma unroll
-      for (int i = 0; i < OPL; ++i) o[j][i] = 0.f;
-    }
-    float* pw = pbuf + h * kStepTokens * G;
-    int slot = 0;
-    uint32_t phase = 0u;
-    bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      const int t0 = t_begin + s * kStepTokens;
-      const int nt = min(kStepTokens, t_end - t0);
-      ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint8_t* kst = smem + slot * stage_bytes;
-      const uint8_t* vst = kst + kStepTokens * row_bytes;
-      const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
-      // Scores of this step's 16 tokens (4 passes of 4 tokens).
-      float sc[4][G];
-#pragma unroll
-      for (int ps = 0; ps < 4; ++ps) {
-        const int t = 4 * ps + tt;
-        float2 acc[G];  // even and odd dims, two lanes of work per packed FMA
-#pragma unroll
-        for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
-        if (t < nt) {
-          const uint8_t* kb = kst + t * row_bytes + (h * D + r * DPL) * 2;
-#pragma unroll
-          for (int c = 0; c < DPL / 8; ++c) {
-            float kf[8];
-            const uint4 w = reinterpret_cast<const uint4*>(kb)[c];
-            bf16x2_to_f32(w.x, kf[0], kf[1]);
-            bf16x2_to_f32(w.y, kf[2], kf[3]);
-            bf16x2_to_f32(w.z, kf[4], kf[5]);
-            bf16x2_to_f32(w.w, kf[6], kf[7]);
-#pragma unroll
-            for (int j = 0; j < G; ++j)
-#pragma unroll
-              for (int e = 0; e < 8; e += 2)
-                acc[j] = ffma2(make_float2(qf[j][8 * c + e], qf[j][8 * c + e + 1]),
-                               make_float2(kf[e], kf[e + 1]), acc[j]);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          float v = acc[j].x + acc[j].y;
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          sc[ps][j] = (t < nt && ((vmask >> t) & 1u)) ? v * sl : -INFINITY;
-        }
-      }
-      // Online softmax, per query head.
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float mx = fmax3(fmaxf(sc[0][j], sc[1][j]), sc[2][j], sc[3][j]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        if (mx > m[j] + 8.0f || (m[j] == -INFINITY && mx != -INFINITY)) {  // warp-uniform
-          const float f = (m[j] == -INFINITY) ? 0.f : ex2_approx(m[j] - mx);
-          lpart[j] *= f;
-#pragma unroll
-          for (int i = 0; i < OPL; ++i) o[j][i] *= f;
-          m[j] = mx;
-        }
-        float ps_sum = 0.f;
-#pragma unroll
-        for (int ps = 0; ps < 4; ++ps) {
-          // (a top-k step may hold no valid entry before any valid one: m = -inf)
-          const float pv = (SP && m[j] == -INFINITY) ? 0.f : ex2_approx(sc[ps][j] - m[j]);
-          ps_sum += pv;
-          if (r == 0) pw[(4 * ps + tt) * G + j] = pv;
-        }
-        if (r == 0) lpart[j] += ps_sum;
-      }
-      __syncwarp();
-      // O += P V over the step's tokens.
-      for (int t = 0; t < nt; ++t) {
-        float pv[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) pv[j] = pw[t * G + j];
-        const uint16_t* vr = reinterpret_cast<const uint16_t*>(vst + t * row_bytes + (h * D + lane * OPL) * 2);
-        float vf[OPL];
-        if (OPL == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(vr);
-          bf16x2_to_f32(w.x, vf[0], vf[1 % OPL]);
-          bf16x2_to_f32(w.y, vf[2 % OPL], vf[3 % OPL]);
-        } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vr);
-          bf16x2_to_f32(w, vf[0], vf[1 % OPL]);
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-          for (int i = 0; i < OPL; i += 2) {
-            const float2 r = ffma2(make_float2(pv[j], pv[j]), make_float2(vf[i], vf[i + 1]),
-                                   make_float2(o[j][i], o[j][i + 1]));
-            o[j][i] = r.x;
-            o[j][i + 1] = r.y;
-          }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
-      if (++slot == nstage) {
-        slot = 0;
-        phase ^= 1u;
-      }
-    }
-    if (ok) {
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float l = lpart[j];
-#pragma unroll
-        for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
-        const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
-        const float inv = empty ? 0.f : 1.f / l;
-        const float lse_v = empty ? -INFINITY : m[j] * kLn2d + logf(l);
-        const int hq = h * G + j;
-        if (n_splits == 1) {
-          uint16_t* dst = p.out + (static_cast<int64_t>(row.q_row) * p.heads + hq) * D + lane * OPL;
-          if (OPL == 4) {
-            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o[j][0] * inv, o[j][1 % OPL] * inv),
-                                                        pack_bf16x2(o[j][2 % OPL] * inv, o[j][3 % OPL] * inv));
-          } else {
-            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[j][0] * inv, o[j][1 % OPL] * inv);
-          }
-          if (p.lse && lane == 0) p.lse[static_cast<int64_t>(hq) * p.lse_stride + row.q_row] = lse_v;
-        } else {
-          float* dst = p.ws_o + (static_cast<int64_t>(item) * p.heads + hq) * D + lane * OPL;
-#pragma unroll
-          for (int i = 0; i < OPL; ++i) dst[i] = o[j][i] * inv;
-          if (lane == 0) p.ws_lse[static_cast<int64_t>(item) * p.heads + hq] = lse_v;
         }
       }
     }
@@ -853,8 +746,7 @@ bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads) 
   if (head_dim_qk != head_dim_v || (head_dim_qk != 64 && head_dim_qk != 128)) return false;
   if (kv_heads < 1 || kv_heads > 8 || heads % kv_heads) return false;
   const int g = heads / kv_heads;
-  // (128, 8) would hold 128 query values per lane and spill: the chunk kernel serves it.
-  return g == 1 || g == 2 || g == 4 || (g == 8 && head_dim_qk == 64);
+  return g == 1 || g == 2 || g == 4 || g == 8;
 }
 
 template <bool F8, bool SP>
@@ -864,6 +756,7 @@ cudaError_t launch_f(const DecodeParams& p, int items, int head_dim, int num_sms
     if (g == 1) return launch_t<128, 1, F8, SP>(p, items, num_sms, stream);
     if (g == 2) return launch_t<128, 2, F8, SP>(p, items, num_sms, stream);
     if (g == 4) return launch_t<128, 4, F8, SP>(p, items, num_sms, stream);
+    if (g == 8) return launch_t<128, 8, F8, SP>(p, items, num_sms, stream);
   } else if (head_dim == 64) {
     if (g == 1) return launch_t<64, 1, F8, SP>(p, items, num_sms, stream);
     if (g == 2) return launch_t<64, 2, F8, SP>(p, items, num_sms, stream);

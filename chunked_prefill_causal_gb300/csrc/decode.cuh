@@ -53,7 +53,7 @@ struct DecodeParams {
 constexpr int kDecodeSplitTokens = 1024;
 
 // True when the decode kernel handles this shape (dq = dv in {64, 128},
-// kv_heads <= 8, heads / kv_heads in {1, 2, 4}, or 8 when dq = 64).
+// kv_heads <= 8, heads / kv_heads in {1, 2, 4, 8}).
 bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads);
 
 // fp8: the cache holds E4M3 codes with per-kv-head k_scale / v_scale.

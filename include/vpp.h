@@ -336,8 +336,8 @@ size_t vpp_mixed_attn_fp8_workspace_size(const int32_t *cu_seqlens_q,
  * lse = -inf.  Cache: bf16, paged (block_table of the one sequence) or
  * contiguous (block_table NULL, num_blocks = capacity in tokens); the keys up
  * to prefix_len + chunk_len - 1 must be in it.  Shapes: those of the decode
- * kernel (head_dim 64 or 128, kv_heads <= 8, heads/kv_heads 1, 2, 4, or 8
- * with head_dim 64); others return VPP_ERR_UNSUPPORTED.  workspace >=
+ * kernel (head_dim 64 or 128, kv_heads <= 8, heads/kv_heads 1, 2, 4 or 8);
+ * others return VPP_ERR_UNSUPPORTED.  workspace >=
  * vpp_topk_chunk_attn_workspace_size(...) (0 when topk <= 1024).
  */
 int vpp_topk_chunk_attn(const void *q, const void *k_cache,

@@ -98,10 +98,10 @@ def test_host_validation_rejects_bad_arguments(lib):
 def test_topk_validation_and_workspace(lib):
     null = None
     fake = ctypes.c_void_p(0x100000)
-    # no index list / unsupported shape (d 128 with 8 query heads per kv head) / bad topk
+    # no index list / unsupported shape (16 query heads per kv head) / bad topk
     assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, null, fake, 2048, 8, 2, 128, 0.0, fake,
                                    null, null, 0, null) == vpp.VPP_ERR_INVALID
-    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 2048, 64, 8, 128, 0.0, fake,
+    assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 2048, 128, 8, 128, 0.0, fake,
                                    null, null, 0, null) == vpp.VPP_ERR_UNSUPPORTED
     assert lib.vpp_topk_chunk_attn(fake, fake, fake, fake, 64, 0, 16, fake, fake, 0, 8, 2, 128, 0.0, fake,
                                    null, null, 0, null) == vpp.VPP_ERR_INVALID

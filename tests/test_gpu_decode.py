@@ -27,7 +27,7 @@ def _gen(shape, seed, std):
     return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (16, 8, 64), (64, 8, 64),
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (16, 8, 64), (64, 8, 64), (64, 8, 128),
                                       (8, 2, 128), (4, 1, 64), (128, 8, 128), (16, 16, 64)])
 def test_decode_rows_match_oracle(Hq, Hkv, d):
     B = len(CTX)

@@ -282,7 +282,7 @@ def _mixed(ctx, qlen, Hq, Hkv, d, seed, qmul=1.0):
     assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (64, 8, 64), (4, 1, 64), (128, 8, 128)])
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (64, 8, 64), (64, 8, 128), (4, 1, 64), (128, 8, 128)])
 def test_fp8_decode_rows_match_oracle(Hq, Hkv, d):
     _mixed(CTX, [1] * len(CTX), Hq, Hkv, d, seed=Hq + d)
 
