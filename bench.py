@@ -450,56 +450,137 @@ def measure_fp8(dev, stream, hbm, w, chunks):
     return out
 
 
+class TopkSetup:
+    """The dsa128k workload resident in HBM for top-k sparse prefix attention:
+    every chunk's q, the whole context's K/V in a bf16 and an E4M3 paged cache,
+    and each chunk's index rows (TOPK listed keys per query token)."""
+
+    def __init__(self, dev):
+        from chunked_prefill_causal_gb300 import vpp
+        w = W.WORKLOADS["dsa128k"]
+        self.w = w
+        self.chunks = w.chunks()
+        nb = W.blocks_for(w.seq_len)
+        self.table = torch.from_numpy(W.block_table(nb, nb + 8, w.seed + 99)).to(dev)
+        self.kc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
+        self.vc = torch.zeros_like(self.kc)
+        self.kc8 = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.uint8, device=dev)
+        self.vc8 = torch.zeros_like(self.kc8)
+        # |k|, |v| < 0.5 in this recipe: 0.5 maps to 448
+        self.s8 = torch.full((w.kv_heads,), 0.5 / 448.0, dtype=torch.float32, device=dev)
+        self.qs, self.idx, self.lens = [], [], []
+        for ci, (p0, c0) in enumerate(self.chunks):
+            qi, ki, vi = W.chunk_tensors(w, ci, dev)
+            vpp.vpp_kv_append(ki, vi, self.kc, self.vc, p0, block_table=self.table)
+            vpp.vpp_kv_append_fp8(ki, vi, self.kc8, self.vc8, self.s8, self.s8, p0, block_table=self.table)
+            self.qs.append(qi)
+            del ki, vi
+            idx, lens = W.topk_indices(p0, c0, W.TOPK, ci, device=dev)
+            self.idx.append(idx)
+            self.lens.append(lens)
+        self.out = torch.empty((w.chunk, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(max(vpp.topk_chunk_attn_workspace_size(w.chunk, W.TOPK, w.heads, w.head_dim_qk), 256),
+                              dtype=torch.uint8, device=dev)
+
+    def gathered_bytes(self, ci, fp8=False):
+        """Algorithmic bytes of chunk ci: every listed key's K and V rows, all
+        kv heads, once per query token that lists it."""
+        w = self.w
+        n_listed = int(self.lens[ci].to(torch.int64).sum())
+        return n_listed * w.kv_heads * (w.head_dim_qk + w.head_dim_v) * (1 if fp8 else 2)
+
+    def run(self, ci, fp8=False):
+        from chunked_prefill_causal_gb300 import vpp
+        P, C = self.chunks[ci]
+        if fp8:
+            vpp.vpp_topk_chunk_attn_fp8(self.qs[ci], self.kc8, self.vc8, self.s8, self.s8, P, self.idx[ci],
+                                        self.lens[ci], block_table=self.table, out=self.out[:C], workspace=self.ws)
+        else:
+            vpp.vpp_topk_chunk_attn(self.qs[ci], self.kc, self.vc, P, self.idx[ci], self.lens[ci],
+                                    block_table=self.table, out=self.out[:C], workspace=self.ws)
+
+
 def measure_topk(dev, stream, hbm, peak_tf):
     """Top-k sparse prefix attention (DSA-style) on the dsa128k workload
     (32/8 heads, d 128, 8 chunks of 16384, TOPK listed keys per query token)
     against dense chunk attention on the same shapes, and the two-rank
     schedules simulated on each set of per-chunk latencies."""
     from chunked_prefill_causal_gb300 import vpp
-    w = W.WORKLOADS["dsa128k"]
-    chunks = w.chunks()
-    nb = W.blocks_for(w.seq_len)
-    table = torch.from_numpy(W.block_table(nb, nb + 8, w.seed + 99)).to(dev)
-    kc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros_like(kc)
-    kc8 = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.uint8, device=dev)
-    vc8 = torch.zeros_like(kc8)
-    s8 = torch.full((w.kv_heads,), 0.5 / 448.0, dtype=torch.float32, device=dev)  # |k|, |v| < 0.5 here
-    qs = []
-    for ci, (p0, c0) in enumerate(chunks):
-        qi, ki, vi = W.chunk_tensors(w, ci, dev)
-        vpp.vpp_kv_append(ki, vi, kc, vc, p0, block_table=table)
-        vpp.vpp_kv_append_fp8(ki, vi, kc8, vc8, s8, s8, p0, block_table=table)
-        qs.append(qi)
-        del ki, vi
-    out = torch.empty((w.chunk, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
-    ws_t = torch.empty(max(vpp.topk_chunk_attn_workspace_size(w.chunk, W.TOPK, w.heads, w.head_dim_qk), 256),
-                       dtype=torch.uint8, device=dev)
+    ts_ = TopkSetup(dev)
+    w = ts_.w
     rows, sparse_ms, dense_ms = [], [], []
-    for ci, (P, C) in enumerate(chunks):
-        idx, lens = W.topk_indices(P, C, W.TOPK, ci, device=dev)
-        ts = time_events(lambda: vpp.vpp_topk_chunk_attn(qs[ci], kc, vc, P, idx, lens, block_table=table,
-                                                         out=out[:C], workspace=ws_t), 5, stream)
-        ts8 = time_events(lambda: vpp.vpp_topk_chunk_attn_fp8(qs[ci], kc8, vc8, s8, s8, P, idx, lens,
-                                                              block_table=table, out=out[:C], workspace=ws_t),
-                          5, stream)
-        td = time_events(lambda: vpp.vpp_chunk_attn_ex(qs[ci], kc, vc, P, block_table=table, out=out[:C],
-                                                       num_splits=1), 3, stream)
-        n_listed = int(lens.to(torch.int64).sum())
-        byts = n_listed * w.kv_heads * (w.head_dim_qk + w.head_dim_v) * 2
+    for ci, (P, C) in enumerate(ts_.chunks):
+        ts = time_events(lambda: ts_.run(ci), 5, stream)
+        ts8 = time_events(lambda: ts_.run(ci, fp8=True), 5, stream)
+        td = time_events(lambda: vpp.vpp_chunk_attn_ex(ts_.qs[ci], ts_.kc, ts_.vc, P, block_table=ts_.table,
+                                                       out=ts_.out[:C], num_splits=1), 3, stream)
+        n_listed = int(ts_.lens[ci].to(torch.int64).sum())
+        byts = ts_.gathered_bytes(ci)
         fl = 2.0 * (w.head_dim_qk + w.head_dim_v) * w.heads * n_listed
         dfl = 2.0 * (w.head_dim_qk + w.head_dim_v) * w.heads * (C * P + C * (C + 1) // 2)
         sparse_ms.append(ts)
         dense_ms.append(td)
         rows.append({"k": ci, "prefix": P, "sparse_ms": round(ts, 3), "dense_ms": round(td, 3),
                      "gathered_gb": round(byts / 1e9, 2), "sparse_gbs": round(byts / (ts / 1e3) / 1e9, 1),
-                     "sparse_frac_hbm": round(byts / (ts / 1e3) / 1e9 / hbm, 4),
                      "sparse_fp8_ms": round(ts8, 3), "sparse_fp8_gbs": round(byts / 2 / (ts8 / 1e3) / 1e9, 1),
                      "sparse_tflops": round(fl / (ts / 1e3) / 1e12, 1),
                      "dense_tflops": round(dfl / (td / 1e3) / 1e12, 1)})
+    if vpp.vpp_last_device_status() != 0:
+        raise RuntimeError("device status word reported an error")
     return {"workload": f"dsa128k: 32/8 heads, d 128, 8 chunks of 16384, {W.TOPK} listed keys per query token",
+            "gathered": "each listed key's K and V rows once per query token that lists it; tokens share keys, "
+                        "so part of it is served from L2 and the rate can exceed the HBM copy peak",
             "per_chunk": rows,
             "schedule_dense": schedule_summary(dense_ms), "schedule_sparse": schedule_summary(sparse_ms)}
+
+
+def run_topk(args, dist_):
+    """Top-k sparse prefix attention of dsa128k as the step: the chunks named
+    by --topk-chunks (default all 8), one vpp_topk_chunk_attn[_fp8] launch each
+    over the cache of the whole context.  Reports gathered bytes per second."""
+    from chunked_prefill_causal_gb300 import vpp
+
+    dist_.init()
+    dev = torch.device("cuda", dist_.local)
+    torch.cuda.set_device(dev)
+    vpp.load()
+    stream = torch.cuda.current_stream()
+    fp8 = args.kv_dtype == "fp8"
+    ts_ = TopkSetup(dev)
+    sel = [int(c) for c in args.topk_chunks.split(",")] if args.topk_chunks else list(range(len(ts_.chunks)))
+    if any(c < 0 or c >= len(ts_.chunks) for c in sel):
+        raise SystemExit(f"--topk-chunks: chunk indices are 0..{len(ts_.chunks) - 1}")
+
+    def step():
+        for ci in sel:
+            ts_.run(ci, fp8)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dist_.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist_.barrier()
+    if vpp.vpp_last_device_status() != 0:
+        raise RuntimeError("device status word reported an error")
+    el = dist_.max(e0.elapsed_time(e1) / 1e3)
+    byts = sum(ts_.gathered_bytes(ci, fp8) for ci in sel)
+    if dist_.rank == 0:
+        print(json.dumps({
+            "metric": "top-k gathered bytes per second", "value": byts * args.steps * dist_.world / el / 1e9,
+            "unit": "GB/s", "n_gpus": dist_.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8" if fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": "dsa128k top-k", "chunks": sel, "topk": W.TOPK, "heads": ts_.w.heads,
+                       "kv_heads": ts_.w.kv_heads, "head_dim": ts_.w.head_dim_qk,
+                       "kv_cache": "E4M3 codes, per-kv-head scales" if fp8 else "bf16"}}), flush=True)
+    return 0
 
 
 def measure_cost_model(dev, stream, n_batches=48, n_train=32, seed=11):
@@ -877,7 +958,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + ["mixed"], default="long128k")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + ["mixed", "topk"], default="long128k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
@@ -885,7 +966,9 @@ def main(argv=None):
     ap.add_argument("--decode-rows", type=int, default=None,
                     help="with --workload mixed: decode rows of the micro-batch (default 256)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="with --workload mixed: the KV cache's element type")
+                    help="with --workload mixed or topk: the KV cache's element type")
+    ap.add_argument("--topk-chunks", default=None,
+                    help="with --workload topk: comma-separated dsa128k chunk indices (default all)")
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=256)
@@ -895,11 +978,13 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     dist_ = Dist()
     if args.impl == "reference":
-        if args.workload == "mixed":
+        if args.workload in ("mixed", "topk"):
             args.workload = "long128k"
         return run_reference(args, dist_)
     if args.workload == "mixed":
         return run_mixed(args, dist_)
+    if args.workload == "topk":
+        return run_topk(args, dist_)
     return run_ours(args, dist_)
 
 

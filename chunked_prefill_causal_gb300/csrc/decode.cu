@@ -39,12 +39,13 @@
 // Top-k mode (SP): the rows are the query tokens of one prefill chunk and each
 // attends only the key positions its index row lists (DSA-style sparse
 // attention: VPP technical review §7; "02 · 并行策略与 PP 切分" §5.1).  A work
-// item is (token, range of 1024 list entries).  bf16: the producer warp
-// gathers a step's 16 listed keys with one bulk copy per key for K and one for
-// V (all kv heads of a key are contiguous).  fp8: each kv-head warp gathers its
-// own slices with 16-byte copies (sp_issue).  Entries outside 0 .. position,
-// or in a block outside the pool, are zero-filled, masked out of the softmax
-// and reported as VPP_ERR_INVALID.
+// item is (token, range of 1024 list entries, head group): the kv heads are
+// split over CTAs of at most 4 (bf16) or 8 (fp8) heads, so that 1 KB rows make
+// 33 KB stages and two CTAs share an SM.  Two gather warps issue a step's 16
+// listed keys as one bulk copy per key for K and one for V, with the list and
+// block-table loads resolved a group of steps ahead.  Entries outside
+// 0 .. position, or in a block outside the pool, are zero-filled, masked out
+// of the softmax and reported as VPP_ERR_INVALID.
 #include <algorithm>
 
 #include "common.cuh"
@@ -55,14 +56,16 @@ namespace vpp {
 namespace {
 
 constexpr int kStepTokens = 16;
+constexpr int kGatherWarps = 2;  // top-k: warps issuing a step's per-key copies
 // Stage ring: six fp8 stages (32 rows of 1 KB + 128 bytes of group padding)
 // or three bf16 stages of 64 KB, for 8 kv heads of d 128.
 constexpr int kDecodeRing = 6 * (32 * 1024 + 128);
-// fp8: half the ring (three stages), so that two CTAs share an SM: decode
-// rows measured 6% faster, and top-k gathers 1.6x faster, than with one CTA
-// and six stages.  (bf16 stages are 64 KB: one CTA per SM.)
-template <bool F8> constexpr int ring_bytes() { return F8 ? kDecodeRing / 2 : kDecodeRing; }
-template <bool F8> constexpr int smem_bytes() { return ring_bytes<F8>() + 4096 + 256; }  // + p exchange, barriers
+// fp8 and top-k: half the ring, three stages of up to 16 + 16 rows of 1 KB
+// (fp8 over 8 kv heads, bf16 over 4), so that two CTAs share an SM: fp8 decode
+// rows measured 6% faster than with one CTA and six stages.  (bf16 decode
+// stages are 64 KB: one CTA per SM.)
+template <bool F8, bool SP> constexpr int ring_bytes() { return (F8 || SP) ? 3 * (32 * 1024 + 256) : kDecodeRing; }
+template <bool F8, bool SP> constexpr int smem_bytes() { return ring_bytes<F8, SP>() + 4096 + 256; }  // + p exchange, barriers
 constexpr float kLn2d = 0.69314718055994530942f;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -70,26 +73,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared through the load/store path;
-// the bytes past src_bytes (16 or 0) are written as zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most n of this thread's copy groups are pending (n < 8).
-__device__ __forceinline__ void cp_async_wait(int n) {
-  switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-  }
 }
 
 __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
@@ -139,11 +122,16 @@ __device__ __forceinline__ int v_row(int t, int row_bytes, int vgroup) {
 }
 
 template <int D, int G, bool F8, bool SP>
-__global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288, (F8 || SP) ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int ESZ = F8 ? 1 : 2;  // cache bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
-  const int hkv = p.kv_heads;
-  const int row_bytes = hkv * D * ESZ;               // one token, all kv heads
+  // Top-k items may split their kv heads over head_groups CTAs: this CTA
+  // serves kv heads h0 .. h0 + hkv - 1.
+  const int hgrp = SP ? static_cast<int>(blockIdx.x % p.head_groups) : 0;
+  const int hkv = SP ? p.kv_heads / p.head_groups : p.kv_heads;
+  const int h0 = hgrp * hkv;
+  const int grow = p.kv_heads * D * ESZ;             // one token, all kv heads (global)
+  const int row_bytes = hkv * D * ESZ;               // one token, this CTA's kv heads (stage)
   // A stage holds a step's 16 K rows as they lie in the cache (one bulk
   // copy), then its V rows in four groups of 4 tokens, vgroup bytes apart.
   // bf16: the groups are contiguous (one copy).  fp8: each group is its own
@@ -153,7 +141,7 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
   // instead needs 32 copies per step, which measured 1.6x slower.)
   const int vgroup = 4 * row_bytes + (F8 ? 32 : 64);
   const int stage_bytes = kStepTokens * row_bytes + 4 * vgroup;
-  constexpr int kRing = ring_bytes<F8>();
+  constexpr int kRing = ring_bytes<F8, SP>();
   const int nstage = min(8, kRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kRing);  // [hkv][16][G]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing + 8 * kStepTokens * 8 * 4);
@@ -163,7 +151,7 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------- work item
-  const int item = blockIdx.x;
+  const int item = SP ? static_cast<int>(blockIdx.x / p.head_groups) : static_cast<int>(blockIdx.x);
   DecodeRow row;
   int split, n_splits, t_begin, t_end;
   const int32_t* list = nullptr;  // SP: this token's index row
@@ -201,95 +189,88 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     for (int i = 0; i < nstage; ++i) {
-      mbar_init(smem_u32(&bars[i]), 1);
+      mbar_init(smem_u32(&bars[i]), SP ? kGatherWarps : 1);
       mbar_init(smem_u32(&bars[8 + i]), hkv);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Top-k mode over an fp8 cache: kv-head warp h gathers its own slices (d
-  // bytes per key, 16-byte copies through the load/store path) of step sp's
-  // listed keys into stage slot sl, at the same places as a whole-row copy
-  // would put them, and returns the step's validity mask.  Invalid entries
-  // (outside 0 .. position, or in a block outside the pool) and rows past the
-  // range are zero-filled.  For 1 KB rows this measured ~1.25x faster than
-  // the producer warp's per-key bulk copies; for bf16's 2 KB rows it measured
-  // 1.2x slower, so bf16 keeps the producer (warp_gather below).
-  auto sp_issue = [&](int h, int sp, int sl) -> uint32_t {
-    const int t0 = t_begin + sp * kStepTokens;
-    const int nt = min(kStepTokens, t_end - t0);
-    int64_t src_row = 0;
-    bool valid = false;
-    if (lane < nt) {
-      const int64_t key = __ldg(list + t0 + lane);
-      if (key >= 0 && key <= pos) {
-        if (p.block_table) {
-          const int32_t blk = __ldg(p.block_table + key / kBlockTokens);
-          valid = blk >= 0 && blk < p.num_blocks;
-          src_row = static_cast<int64_t>(blk) * kBlockTokens + key % kBlockTokens;
-        } else {
-          valid = key < p.num_blocks;  // contiguous cache: num_blocks is the capacity in tokens
-          src_row = key;
-        }
-      }
-      if (!valid && h == 0) record_status(p.status, kStatusInvalid);
-    }
-    const uint32_t vm = __ballot_sync(0xffffffffu, valid && lane < kStepTokens) & 0xFFFFu;
-    constexpr int kChunks = D * ESZ / 16;  // 16-byte pieces of one key's slice
-    constexpr int kKeys = 32 / kChunks;    // keys per warp instruction
-    const int c = lane % kChunks;
-    const int kk = lane / kChunks;
-    uint8_t* stage = smem + sl * stage_bytes;
-    const uint8_t* kb = static_cast<const uint8_t*>(p.k_cache) + h * D * ESZ + c * 16;
-    const uint8_t* vb = static_cast<const uint8_t*>(p.v_cache) + h * D * ESZ + c * 16;
+  if (SP && warp >= hkv) {
+    // ------------------------------------------------------ gather warps
+    // kGatherWarps warps share a step's 32 copies, the K row (c < 16) and the
+    // V row (c >= 16) of each of its 16 listed keys: copy c is issued by lane
+    // c / kGatherWarps of gather warp c % kGatherWarps.  The rows of the list
+    // entries are resolved ahead, a group of 8 steps (128 entries) at a time
+    // (lane l holds entries l + 32 j of a group): while group g is copied,
+    // the block-table entries of group g + 1 and the list entries of group
+    // g + 2 are in flight, so that these dependent loads stay off the copy
+    // path.  Every gather warp resolves the rows itself and arrives on the
+    // stage's full barrier with its own bytes.
+    const int gw = warp - hkv;
+    const int c = gw + kGatherWarps * lane;  // this lane's copy (c < 32)
+    const int t = c & 15;
+    const bool is_v = c >= 16;
+    int32_t key_a[4], blk_a[4], key_b[4];  // group g + 1: keys, table entries; group g + 2: keys
+    int64_t row_c[4];                      // group g: source rows, -1 if invalid or past the range
+    auto load_keys = [&](int grp, int32_t (&k)[4]) {
 #pragma unroll
-    for (int i = 0; i < kStepTokens / kKeys; ++i) {
-      const int t = i * kKeys + kk;
-      const int64_t r = __shfl_sync(0xffffffffu, src_row, t);
-      const bool v = (vm >> t) & 1u;
-      const int64_t off = (v ? r : 0) * row_bytes;
-      cp_async16(smem_u32(stage + t * row_bytes + h * D * ESZ + c * 16), kb + off, v ? 16u : 0u);
-      cp_async16(smem_u32(stage + v_row<F8>(t, row_bytes, vgroup) + h * D * ESZ + c * 16), vb + off,
-                 v ? 16u : 0u);
-    }
-    cp_async_commit();
-    return vm;
-  };
-  const int sp_ahead = nstage - 1;  // steps gathered ahead of the one computed
-  constexpr bool warp_gather = SP && F8;
-
-
-  if (SP && warp == hkv) {
-    // ------------------------------------------------------ producer (gather)
-    if (warp_gather) return;  // the kv-head warps gather their own slices (sp_issue)
-    // Lane t < 16 fetches the K row of list entry t0 + t, lane 16 + t its V row.
+      for (int j = 0; j < 4; ++j) {
+        const int e = t_begin + grp * 128 + 32 * j + lane;
+        k[j] = e < t_end ? __ldg(list + e) : -1;
+      }
+    };
+    auto load_blocks = [&](const int32_t (&k)[4], int32_t (&bk)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        bk[j] = (p.block_table && k[j] >= 0 && k[j] <= pos) ? __ldg(p.block_table + k[j] / kBlockTokens) : 0;
+    };
+    auto resolve = [&](int grp) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = t_begin + grp * 128 + 32 * j + lane;
+        const int64_t key = key_a[j];
+        bool valid = false;
+        int64_t r = -1;
+        if (key >= 0 && key <= pos) {
+          if (p.block_table) {
+            valid = blk_a[j] >= 0 && blk_a[j] < p.num_blocks;
+            r = static_cast<int64_t>(blk_a[j]) * kBlockTokens + key % kBlockTokens;
+          } else {
+            valid = key < p.num_blocks;  // contiguous cache: num_blocks is the capacity in tokens
+            r = key;
+          }
+        }
+        if (e < t_end && !valid && gw == 0) record_status(p.status, kStatusInvalid);
+        row_c[j] = (e < t_end && valid) ? r : -1;
+      }
+    };
+    load_keys(0, key_a);
+    load_blocks(key_a, blk_a);
+    load_keys(1, key_b);
     int slot = 0;
     uint32_t phase = 0u;
     uint32_t filled = 0u, fill_phase = 0u;
     bool ok = true;
-    const int t = lane & 15;
-    const bool is_v = lane >= 16;
     for (int s = 0; s < n_steps; ++s) {
+      if ((s & 7) == 0) {
+        resolve(s >> 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key_a[j] = key_b[j];
+        load_blocks(key_a, blk_a);
+        load_keys((s >> 3) + 2, key_b);
+      }
       const int t0 = t_begin + s * kStepTokens;
       const int nt = min(kStepTokens, t_end - t0);
-      bool valid = false;
-      int64_t src_row = 0;
-      if (t < nt) {
-        const int64_t key = __ldg(list + t0 + t);
-        if (key >= 0 && key <= pos) {
-          if (p.block_table) {
-            const int32_t blk = __ldg(p.block_table + key / kBlockTokens);
-            valid = blk >= 0 && blk < p.num_blocks;
-            src_row = static_cast<int64_t>(blk) * kBlockTokens + key % kBlockTokens;
-          } else {
-            valid = key < p.num_blocks;  // contiguous cache: num_blocks is the capacity in tokens
-            src_row = key;
-          }
-        }
-        if (!valid && !is_v) record_status(p.status, kStatusInvalid);
-      }
-      const uint32_t vmask = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;  // K lanes decide
+      const int kq = (s & 7) >> 1;
+      const int64_t mine = kq == 0 ? row_c[0] : kq == 1 ? row_c[1] : kq == 2 ? row_c[2] : row_c[3];
+      // the step's validity word (lane l < 16: entry l), then this lane's row
+      const int64_t rl = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + (lane & 15));
+      const uint32_t vmask = __ballot_sync(0xffffffffu, lane < 16 && rl >= 0) & 0xFFFFu;
+      const int64_t src_row = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + t);
+      const bool mine_in = c < 32 && t < nt;
+      const bool valid = mine_in && ((vmask >> t) & 1u);
+      const uint32_t cmask = __ballot_sync(0xffffffffu, valid);
       bool w_ok = true;
       if (lane == 0) w_ok = mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag);
       if (!__shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0)) {
@@ -297,20 +278,20 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
         break;
       }
       uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8>(t, row_bytes, vgroup) : t * row_bytes);
-      if (t < nt && !valid) {  // zero-filled, so that P = 0 times it stays 0
+      if (mine_in && !valid) {  // zero-filled, so that P = 0 times it stays 0
         for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();  // before later bulk copies into these bytes
       }
       __syncwarp();
       const uint32_t full = smem_u32(&bars[slot]);
       if (lane == 0) {
-        step_valid[slot] = vmask;
-        mbar_arrive_expect_tx(full, 2u * static_cast<uint32_t>(__popc(vmask)) * row_bytes);
+        if (gw == 0) step_valid[slot] = vmask;
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(cmask)) * row_bytes);
       }
       __syncwarp();
-      if (t < nt && valid) {
+      if (valid) {
         const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
-        bulk_g2s(smem_u32(dstp), base + src_row * row_bytes, static_cast<uint32_t>(row_bytes), full);
+        bulk_g2s(smem_u32(dstp), base + src_row * grow + h0 * D * ESZ, static_cast<uint32_t>(row_bytes), full);
       }
       filled |= 1u << slot;
       fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
@@ -391,7 +372,7 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
     uint32_t qb[KS][2];
     float qscale = 1.f;  // fp8: 2^-e of head gq
     const uint4* qsrc = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D + u * (D / 4));
+        p.q + (static_cast<int64_t>(row.q_row) * p.heads + (h0 + h) * G + min(gq, G - 1)) * D + u * (D / 4));
     if (!F8) {
       // bf16 operands: q's pairs are the B fragment as they are.
       uint32_t qw[D / 8];
@@ -437,10 +418,10 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
       }
     }
     // This thread's S^T columns are heads 2u and 2u + 1.
-    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
+    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h0 + h) : p.scale_log2;
     const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
                           sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
-    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
+    const float vsc = F8 ? __ldg(p.v_scale + h0 + h) : 1.f;
     float m[2] = {-INFINITY, -INFINITY};
     float lpart[2] = {0.f, 0.f};
     float o[KS][4];
@@ -450,40 +431,14 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
     int slot = 0;
     uint32_t phase = 0u;
     bool ok = true;
-    uint32_t my_vm = 0u;  // warp_gather: lane i < nstage holds the validity mask of stage slot i
-    if (warp_gather) {
-      for (int sp = 0; sp < sp_ahead; ++sp) {
-        if (sp < n_steps) {
-          const uint32_t vm = sp_issue(h, sp, sp);
-          if (lane == sp) my_vm = vm;
-        } else {
-          cp_async_commit();
-        }
-      }
-    }
     for (int s = 0; s < n_steps; ++s) {
       const int t0 = t_begin + s * kStepTokens;
       const int nt = min(kStepTokens, t_end - t0);
-      if (warp_gather) {
-        // gather the step sp_ahead ahead into the slot computed last, then
-        // wait for this step's copies
-        const int spf = s + sp_ahead;
-        const int slf = spf % nstage;
-        if (spf < n_steps) {
-          const uint32_t vm = sp_issue(h, spf, slf);
-          if (lane == slf) my_vm = vm;
-        } else {
-          cp_async_commit();
-        }
-        cp_async_wait(sp_ahead);
-        __syncwarp();
-      } else {
-        ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
+      ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       const uint8_t* kst = smem + slot * stage_bytes;
-      const uint32_t vmask = warp_gather ? __shfl_sync(0xffffffffu, my_vm, slot) : (SP ? step_valid[slot] : 0xFFFFu);
+      const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
       // ---- S^T = K Q^T (two accumulator chains)
       // A thread reads KW words (D/4 elements) of each of its two token rows.
       // Rows lie a multiple of 128 bytes apart, so a quarter warp's two
@@ -627,7 +582,7 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
         }
       }
       __syncwarp();
-      if (!warp_gather && lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
       if (++slot == nstage) {
         slot = 0;
         phase ^= 1u;
@@ -645,7 +600,7 @@ __global__ void __launch_bounds__(288, F8 ? 2 : 1) decode_kernel(const __grid_co
         const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
         const float inv = empty ? 0.f : vsc / l;
         const float lse_v = empty ? -INFINITY : m[hh] * kLn2d + logf(l);
-        const int hq = h * G + j;
+        const int hq = (h0 + h) * G + j;
         // dims gq D/8 + 2i (o[i][hh]) and + 2i + 1 (o[i][2 + hh])
         if (n_splits == 1) {
           uint32_t pk[KS];
@@ -731,11 +686,12 @@ cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
     e = cudaFuncSetAttribute(decode_kernel<D, G, F8, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<F8>());
+                             smem_bytes<F8, SP>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  decode_kernel<D, G, F8, SP><<<items, 32 * (p.kv_heads + 1), smem_bytes<F8>(), st>>>(p);
+  const int warps = SP ? p.kv_heads / p.head_groups + kGatherWarps : p.kv_heads + 1;
+  decode_kernel<D, G, F8, SP><<<items, 32 * warps, smem_bytes<F8, SP>(), st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = SP ? p.topk_tokens : static_cast<int64_t>(p.n_rows);
