@@ -67,6 +67,11 @@ CASES = [  # Hq, Hkv, d, P, C, topk, paged
     (4, 4, 64, 700, 50, 300, True),       # G = 1
     (8, 1, 64, 2000, 40, 1100, True),     # G = 8, d 64
     (4, 2, 128, 100, 33, 7, True),        # G = 2, lists shorter than one 16-key step
+    # bf16 items split their kv heads over CTAs of at most 4 (head groups)
+    (16, 8, 128, 1500, 70, 2048, True),   # 2 groups of 4 kv heads
+    (12, 6, 64, 900, 45, 1200, False),    # 2 groups of 3, contiguous cache
+    (10, 5, 128, 600, 40, 500, True),     # 5 groups of 1
+    (56, 7, 64, 400, 30, 300, True),      # 7 groups of 1, G = 8
 ]
 
 
@@ -77,8 +82,9 @@ def test_topk_attention_matches_oracle(case):
     run_case(Hq, Hkv, d, P, C, topk, seed=sum(case[:6]) % 991, paged_cache=pg)
 
 
-def test_invalid_entries_are_masked_and_reported():
-    Hq, Hkv, d, P, C, topk = 8, 2, 128, 400, 20, 96
+@pytest.mark.parametrize("Hq,Hkv,d,topk", [(8, 2, 128, 96), (16, 8, 64, 300)])
+def test_invalid_entries_are_masked_and_reported(Hq, Hkv, d, topk):
+    P, C = 400, 20
     std = 1 / math.sqrt(d)
     q = gen((C, Hq, d), 61, std)
     k = gen((P + C, Hkv, d), 62, std)
@@ -89,6 +95,10 @@ def test_invalid_entries_are_masked_and_reported():
     bad[0, 3] = -5                       # negative
     bad[1, 10] = P + 1 + 50              # after the query's own position
     bad[2, :lens[2]] = P + C + 10        # every entry beyond the cache: the row is empty
+    if topk > 256:                       # entries in later groups of 128 (resolved ahead of the copies)
+        bad[0, 200] = -1
+        bad[1, 140] = P + 1 + 7
+        bad[1, 299] = P + 1 + 9
     kc, vc, table = paged(k, v, 8)
     lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
     out = vpp.vpp_topk_chunk_attn(q.to(DEV), kc, vc, P, torch.from_numpy(bad).to(DEV),
@@ -135,8 +145,9 @@ def test_bad_list_length_gives_an_empty_row():
         assert_close(got[r:r + 1], ref)
 
 
-def test_topk_over_fp8_cache():
-    Hq, Hkv, d, P, C, topk = 8, 2, 128, 2500, 50, 2048
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (16, 8, 128), (48, 6, 64)])
+def test_topk_over_fp8_cache(Hq, Hkv, d):
+    P, C, topk = 2500, 50, 2048
     std = 1 / math.sqrt(d)
     q = gen((C, Hq, d), 81, std)
     k = gen((P + C, Hkv, d), 82, std)
