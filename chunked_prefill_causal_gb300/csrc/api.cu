@@ -556,13 +556,7 @@ int topk_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache,
     return VPP_ERR_INVALID;
   const int64_t S = ceil_div(topk, kDecodeSplitTokens);
   const int64_t items = C * S;
-  // An item's kv heads are split over head groups (CTAs) of at most 4 (bf16)
-  // or 8 (fp8), so that a CTA's stages (1 KB rows at d 128) are small enough
-  // for two CTAs per SM.
-  const int max_hkv = fp8 ? 8 : 4;
-  int hg = 1;
-  while (kv_heads / hg > max_hkv || kv_heads % hg != 0) ++hg;
-  if (items * hg > INT32_MAX || C > INT32_MAX) return VPP_ERR_INVALID;
+  if (items > INT32_MAX || C > INT32_MAX) return VPP_ERR_INVALID;
   const size_t need = topk_ws_bytes(C, topk, heads, d);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return VPP_ERR_WORKSPACE;
   DeviceState* ds = nullptr;
@@ -593,10 +587,9 @@ int topk_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache,
   dp.topk_len = topk_len;
   dp.topk = topk;
   dp.topk_splits = (int32_t)S;
-  dp.head_groups = hg;
   dp.topk_prefix = P;
   dp.topk_tokens = C;
-  if (launch_decode(dp, (int)(items * hg), d, fp8, true, ds->num_sms, st) != cudaSuccess) return VPP_ERR_CUDA;
+  if (launch_decode(dp, (int)items, d, fp8, true, ds->num_sms, st) != cudaSuccess) return VPP_ERR_CUDA;
   return VPP_OK;
 }
 

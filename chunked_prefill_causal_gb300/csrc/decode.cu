@@ -39,13 +39,12 @@
 // Top-k mode (SP): the rows are the query tokens of one prefill chunk and each
 // attends only the key positions its index row lists (DSA-style sparse
 // attention: VPP technical review §7; "02 · 并行策略与 PP 切分" §5.1).  A work
-// item is (token, range of 1024 list entries, head group): the kv heads are
-// split over CTAs of at most 4 (bf16) or 8 (fp8) heads, so that 1 KB rows make
-// 33 KB stages and two CTAs share an SM.  Two gather warps issue a step's 16
-// listed keys as one bulk copy per key for K and one for V, with the list and
-// block-table loads resolved a group of steps ahead.  Entries outside
-// 0 .. position, or in a block outside the pool, are zero-filled, masked out
-// of the softmax and reported as VPP_ERR_INVALID.
+// item is (token, range of 1024 list entries).  Gather warps (four for bf16,
+// two for fp8) issue a step's 16 listed keys as one bulk copy per key for K
+// and one for V, with the list and block-table loads resolved a group of
+// steps ahead.  Entries outside 0 .. position, or in a block outside the
+// pool, are zero-filled, masked out of the softmax and reported as
+// VPP_ERR_INVALID.
 #include <algorithm>
 
 #include "common.cuh"
@@ -56,16 +55,18 @@ namespace vpp {
 namespace {
 
 constexpr int kStepTokens = 16;
-constexpr int kGatherWarps = 2;  // top-k: warps issuing a step's per-key copies
+// Top-k: warps issuing a step's per-key copies.  One warp issues a bulk copy
+// about every 85 cycles, so bf16's 64 KB steps need four; fp8 (two CTAs per
+// SM) runs best with two.
+template <bool F8> constexpr int gather_warps() { return F8 ? 2 : 4; }
 // Stage ring: six fp8 stages (32 rows of 1 KB + 128 bytes of group padding)
 // or three bf16 stages of 64 KB, for 8 kv heads of d 128.
 constexpr int kDecodeRing = 6 * (32 * 1024 + 128);
-// fp8 and top-k: half the ring, three stages of up to 16 + 16 rows of 1 KB
-// (fp8 over 8 kv heads, bf16 over 4), so that two CTAs share an SM: fp8 decode
-// rows measured 6% faster than with one CTA and six stages.  (bf16 decode
-// stages are 64 KB: one CTA per SM.)
-template <bool F8, bool SP> constexpr int ring_bytes() { return (F8 || SP) ? 3 * (32 * 1024 + 256) : kDecodeRing; }
-template <bool F8, bool SP> constexpr int smem_bytes() { return ring_bytes<F8, SP>() + 4096 + 256; }  // + p exchange, barriers
+// fp8: half the ring, three stages, so that two CTAs share an SM: decode rows
+// measured 6% faster, and top-k gathers 1.2-1.5x faster, than with one CTA and
+// six stages.  (bf16 stages are 64 KB: one CTA per SM.)
+template <bool F8> constexpr int ring_bytes() { return F8 ? kDecodeRing / 2 : kDecodeRing; }
+template <bool F8> constexpr int smem_bytes() { return ring_bytes<F8>() + 4096 + 256; }  // + p exchange, barriers
 constexpr float kLn2d = 0.69314718055994530942f;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -122,16 +123,11 @@ __device__ __forceinline__ int v_row(int t, int row_bytes, int vgroup) {
 }
 
 template <int D, int G, bool F8, bool SP>
-__global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288, (F8 || SP) ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int ESZ = F8 ? 1 : 2;  // cache bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
-  // Top-k items may split their kv heads over head_groups CTAs: this CTA
-  // serves kv heads h0 .. h0 + hkv - 1.
-  const int hgrp = SP ? static_cast<int>(blockIdx.x % p.head_groups) : 0;
-  const int hkv = SP ? p.kv_heads / p.head_groups : p.kv_heads;
-  const int h0 = hgrp * hkv;
-  const int grow = p.kv_heads * D * ESZ;             // one token, all kv heads (global)
-  const int row_bytes = hkv * D * ESZ;               // one token, this CTA's kv heads (stage)
+  const int hkv = p.kv_heads;
+  const int row_bytes = hkv * D * ESZ;               // one token, all kv heads
   // A stage holds a step's 16 K rows as they lie in the cache (one bulk
   // copy), then its V rows in four groups of 4 tokens, vgroup bytes apart.
   // bf16: the groups are contiguous (one copy).  fp8: each group is its own
@@ -141,7 +137,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
   // instead needs 32 copies per step, which measured 1.6x slower.)
   const int vgroup = 4 * row_bytes + (F8 ? 32 : 64);
   const int stage_bytes = kStepTokens * row_bytes + 4 * vgroup;
-  constexpr int kRing = ring_bytes<F8, SP>();
+  constexpr int kRing = ring_bytes<F8>();
   const int nstage = min(8, kRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kRing);  // [hkv][16][G]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing + 8 * kStepTokens * 8 * 4);
@@ -151,7 +147,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
   const int lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------- work item
-  const int item = SP ? static_cast<int>(blockIdx.x / p.head_groups) : static_cast<int>(blockIdx.x);
+  const int item = blockIdx.x;
   DecodeRow row;
   int split, n_splits, t_begin, t_end;
   const int32_t* list = nullptr;  // SP: this token's index row
@@ -189,7 +185,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     for (int i = 0; i < nstage; ++i) {
-      mbar_init(smem_u32(&bars[i]), SP ? kGatherWarps : 1);
+      mbar_init(smem_u32(&bars[i]), SP ? gather_warps<F8>() : 1);
       mbar_init(smem_u32(&bars[8 + i]), hkv);
     }
     fence_mbar_init();
@@ -198,9 +194,9 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
 
   if (SP && warp >= hkv) {
     // ------------------------------------------------------ gather warps
-    // kGatherWarps warps share a step's 32 copies, the K row (c < 16) and the
+    // The gather warps share a step's 32 copies, the K row (c < 16) and the
     // V row (c >= 16) of each of its 16 listed keys: copy c is issued by lane
-    // c / kGatherWarps of gather warp c % kGatherWarps.  The rows of the list
+    // c / NG of gather warp c % NG.  The rows of the list
     // entries are resolved ahead, a group of 8 steps (128 entries) at a time
     // (lane l holds entries l + 32 j of a group): while group g is copied,
     // the block-table entries of group g + 1 and the list entries of group
@@ -208,7 +204,8 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
     // path.  Every gather warp resolves the rows itself and arrives on the
     // stage's full barrier with its own bytes.
     const int gw = warp - hkv;
-    const int c = gw + kGatherWarps * lane;  // this lane's copy (c < 32)
+    constexpr int NG = gather_warps<F8>();
+    const int c = gw + NG * lane;  // this lane's copy (c < 32)
     const int t = c & 15;
     const bool is_v = c >= 16;
     int32_t key_a[4], blk_a[4], key_b[4];  // group g + 1: keys, table entries; group g + 2: keys
@@ -291,7 +288,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
       __syncwarp();
       if (valid) {
         const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
-        bulk_g2s(smem_u32(dstp), base + src_row * grow + h0 * D * ESZ, static_cast<uint32_t>(row_bytes), full);
+        bulk_g2s(smem_u32(dstp), base + src_row * row_bytes, static_cast<uint32_t>(row_bytes), full);
       }
       filled |= 1u << slot;
       fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
@@ -372,7 +369,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
     uint32_t qb[KS][2];
     float qscale = 1.f;  // fp8: 2^-e of head gq
     const uint4* qsrc = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(row.q_row) * p.heads + (h0 + h) * G + min(gq, G - 1)) * D + u * (D / 4));
+        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D + u * (D / 4));
     if (!F8) {
       // bf16 operands: q's pairs are the B fragment as they are.
       uint32_t qw[D / 8];
@@ -418,10 +415,10 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
       }
     }
     // This thread's S^T columns are heads 2u and 2u + 1.
-    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h0 + h) : p.scale_log2;
+    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
     const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
                           sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
-    const float vsc = F8 ? __ldg(p.v_scale + h0 + h) : 1.f;
+    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
     float m[2] = {-INFINITY, -INFINITY};
     float lpart[2] = {0.f, 0.f};
     float o[KS][4];
@@ -600,7 +597,7 @@ __global__ void __launch_bounds__(SP ? 32 * ((F8 ? 8 : 4) + kGatherWarps) : 288,
         const bool empty = !(l > 0.f);  // top-k rows whose entries were all invalid
         const float inv = empty ? 0.f : vsc / l;
         const float lse_v = empty ? -INFINITY : m[hh] * kLn2d + logf(l);
-        const int hq = (h0 + h) * G + j;
+        const int hq = h * G + j;
         // dims gq D/8 + 2i (o[i][hh]) and + 2i + 1 (o[i][2 + hh])
         if (n_splits == 1) {
           uint32_t pk[KS];
@@ -686,12 +683,12 @@ cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
     e = cudaFuncSetAttribute(decode_kernel<D, G, F8, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<F8, SP>());
+                             smem_bytes<F8>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int warps = SP ? p.kv_heads / p.head_groups + kGatherWarps : p.kv_heads + 1;
-  decode_kernel<D, G, F8, SP><<<items, 32 * warps, smem_bytes<F8, SP>(), st>>>(p);
+  const int warps = p.kv_heads + (SP ? gather_warps<F8>() : 1);
+  decode_kernel<D, G, F8, SP><<<items, 32 * warps, smem_bytes<F8>(), st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = SP ? p.topk_tokens : static_cast<int64_t>(p.n_rows);

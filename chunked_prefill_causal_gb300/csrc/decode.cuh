@@ -44,8 +44,6 @@ struct DecodeParams {
   const int32_t* topk_len;     // [n_tokens]
   int32_t topk;                // row stride of topk_idx (the list capacity k)
   int32_t topk_splits;         // work items per token: ceil(k / split_tokens)
-  int32_t head_groups;         // top-k: CTAs sharing a work item's kv heads (groups of kv_heads / head_groups)
-  int32_t pad1;
   int64_t topk_prefix;
   int64_t topk_tokens;
   DecodeRow rows[kMaxBatch];

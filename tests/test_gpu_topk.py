@@ -67,11 +67,11 @@ CASES = [  # Hq, Hkv, d, P, C, topk, paged
     (4, 4, 64, 700, 50, 300, True),       # G = 1
     (8, 1, 64, 2000, 40, 1100, True),     # G = 8, d 64
     (4, 2, 128, 100, 33, 7, True),        # G = 2, lists shorter than one 16-key step
-    # bf16 items split their kv heads over CTAs of at most 4 (head groups)
-    (16, 8, 128, 1500, 70, 2048, True),   # 2 groups of 4 kv heads
-    (12, 6, 64, 900, 45, 1200, False),    # 2 groups of 3, contiguous cache
-    (10, 5, 128, 600, 40, 500, True),     # 5 groups of 1
-    (56, 7, 64, 400, 30, 300, True),      # 7 groups of 1, G = 8
+    # more kv heads per token row (one warp each, 4 gather warps for bf16)
+    (16, 8, 128, 1500, 70, 2048, True),
+    (12, 6, 64, 900, 45, 1200, False),    # contiguous cache
+    (10, 5, 128, 600, 40, 500, True),
+    (56, 7, 64, 400, 30, 300, True),      # G = 8
 ]
 
 
