@@ -115,11 +115,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Offset of V row t in a stage: 16 K rows, then the V rows in four groups of
-// 4 tokens, vgroup bytes apart.
+// Offset of V row t in a stage: the K rows (kbytes), then the V rows in four
+// groups of 4 tokens, each group contiguous and shifted by a few 16-byte
+// units.  The four lanes of a P V fragment group read the same dims of four
+// tokens, one from each group; with the shifts (fp8: 0, 32, 64, 96 bytes;
+// bf16: 0, 16, 64, 80 bytes, whose lanes read 32 bytes in two 16-byte loads)
+// the eight lanes of each quarter warp hit eight different bank groups.
 template <bool F8>
-__device__ __forceinline__ int v_row(int t, int kbytes, int row_bytes, int vgroup) {
-  return kbytes + (t >> 2) * vgroup + (t & 3) * row_bytes;
+__device__ __forceinline__ int v_row(int t, int kbytes, int row_bytes) {
+  const int g = t >> 2;
+  return kbytes + t * row_bytes + (F8 ? 32 * g : 16 * (g & 1) + 64 * (g >> 1));
 }
 
 template <int D, int G, bool F8, bool SP>
@@ -129,18 +134,14 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   const int hkv = p.kv_heads;
   const int row_bytes = hkv * D * ESZ;               // one token, all kv heads
   // A stage holds a step's 16 K rows as they lie in the cache (one bulk
-  // copy), then its V rows in four groups of 4 tokens, vgroup bytes apart.
-  // bf16: the groups are contiguous (one copy).  fp8: each group is its own
-  // copy and the groups are 32 bytes apart, so that the four lanes of a
-  // P V fragment group, which read the same dims of four tokens, read from
-  // four groups and so from four different banks.  (Padding every row
-  // instead needs 32 copies per step, which measured 1.6x slower.)
-  const int vgroup = 4 * row_bytes + (F8 ? 32 : 64);
+  // copy), then its V rows in four groups of 4 tokens (one copy each; see
+  // v_row).  (Padding every V row of a decode step instead needs 32 copies
+  // per step, which measured 1.6x slower.)
   // Top-k K rows are copied one by one: 16 bytes of padding after each puts
   // the rows of a fragment load in different banks.
   const int kstride = SP ? row_bytes + 16 : row_bytes;
   const int kbytes = kStepTokens * kstride;
-  const int stage_bytes = kbytes + 4 * vgroup;
+  const int stage_bytes = kbytes + kStepTokens * row_bytes + 128;
   constexpr int kRing = ring_bytes<F8>();
   const int nstage = min(8, kRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kRing);  // [hkv][16][G]
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
         ok = false;
         break;
       }
-      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8>(t, kbytes, row_bytes, vgroup) : t * kstride);
+      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8>(t, kbytes, row_bytes) : t * kstride);
       if (mine_in && !valid) {  // zero-filled, so that P = 0 times it stays 0
         for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();  // before later bulk copies into these bytes
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
           bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
           const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
           for (int g4 = 0; 4 * g4 < nt; ++g4)
-            bulk_g2s(dst + v_row<F8>(4 * g4, kbytes, row_bytes, vgroup), vsrc + 4 * g4 * row_bytes,
+            bulk_g2s(dst + v_row<F8>(4 * g4, kbytes, row_bytes), vsrc + 4 * g4 * row_bytes,
                      static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
         } else {
           mbar_arrive(full);  // invalid block: the step's rows are skipped
@@ -542,15 +543,11 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int t = 4 * u + q4;
-        const uint8_t* src = kst + v_row<F8>(t, kbytes, row_bytes, vgroup) + (h * D + gq * (D / 8)) * ESZ;
+        const uint8_t* src = kst + v_row<F8>(t, kbytes, row_bytes) + (h * D + gq * (D / 8)) * ESZ;
         uint32_t w[VW];
         if (VW == 8) {
-          // 32 bytes: the two 16-byte pieces in a lane-dependent order (bank
-          // spread across the groups 64 bytes apart), swapped back
-          const int sw = u >> 1;
-          const uint4 wa = reinterpret_cast<const uint4*>(src)[sw];
-          const uint4 wb = reinterpret_cast<const uint4*>(src)[sw ^ 1];
-          const uint4 w0 = sw ? wb : wa, w1 = sw ? wa : wb;
+          const uint4 w0 = reinterpret_cast<const uint4*>(src)[0];
+          const uint4 w1 = reinterpret_cast<const uint4*>(src)[1];
           w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
           w[4 % VW] = w1.x; w[5 % VW] = w1.y; w[6 % VW] = w1.z; w[7 % VW] = w1.w;
         } else if (VW == 4) {
