@@ -61,7 +61,7 @@ constexpr int kStepTokens = 16;
 template <bool F8> constexpr int gather_warps() { return F8 ? 2 : 4; }
 // Stage ring: six fp8 stages (32 rows of 1 KB + group and row padding) or
 // three bf16 stages of 64 KB, for 8 kv heads of d 128.
-constexpr int kDecodeRing = 6 * (32 * 1024 + 512);
+constexpr int kDecodeRing = 6 * (32 * 1024 + 576);
 // fp8: half the ring, three stages, so that two CTAs share an SM: decode rows
 // measured 6% faster, and top-k gathers 1.2-1.5x faster, than with one CTA and
 // six stages.  (bf16 stages are 64 KB: one CTA per SM.)
@@ -137,9 +137,9 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   // copy), then its V rows in four groups of 4 tokens (one copy each; see
   // v_row).  (Padding every V row of a decode step instead needs 32 copies
   // per step, which measured 1.6x slower.)
-  // Top-k K rows are copied one by one: 16 bytes of padding after each puts
-  // the rows of a fragment load in different banks.
-  const int kstride = SP ? row_bytes + 16 : row_bytes;
+  // Top-k K rows are copied one by one: padding after each puts the rows of
+  // a fragment load in different banks (see the K reads).
+  const int kstride = SP ? row_bytes + (F8 ? 16 : 64) : row_bytes;
   const int kbytes = kStepTokens * kstride;
   const int stage_bytes = kbytes + kStepTokens * row_bytes + 128;
   constexpr int kRing = ring_bytes<F8>();
@@ -373,14 +373,18 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     constexpr int KS = D / 16;  // k-steps of S, tiles of O
     uint32_t qb[KS][2];
     float qscale = 1.f;  // fp8: 2^-e of head gq
-    const uint4* qsrc = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D + u * (D / 4));
+    // bf16 top-k: lane u's 16-byte pieces of a row are pieces 4c + u (see the
+    // K reads); otherwise its D/4 elements are contiguous.
+    constexpr bool kInterleaved = SP && !F8;
+    const uint4* qrow = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D);
+    const uint4* qsrc = kInterleaved ? qrow + u : qrow + u * (D / 32);
     if (!F8) {
       // bf16 operands: q's pairs are the B fragment as they are.
       uint32_t qw[D / 8];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 w = gq < G ? __ldg(qsrc + (kInterleaved ? 4 * c : c)) : make_uint4(0u, 0u, 0u, 0u);
         qw[4 * c] = w.x;
         qw[4 * c + 1] = w.y;
         qw[4 * c + 2] = w.z;
@@ -446,16 +450,24 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
       // Decode rows lie a multiple of 128 bytes apart, so a quarter warp's
       // two groups would hit the same banks: the 16-byte pieces are read in
       // an order that depends on the lane (and put back in place by
-      // selects).  Top-k rows are padded to 16 bytes past such a multiple
-      // and read in order: 4-7% faster top-k than the lane-dependent order.
+      // selects).  Top-k rows are copied one by one and padded instead (16
+      // bytes past such a multiple for fp8, 64 for bf16, whose lanes take
+      // interleaved pieces), and read in order: 7-12% faster top-k than the
+      // lane-dependent order.
       constexpr int KW = D * ESZ / 16;  // 32-bit words of a thread's part of one K row
       uint32_t kw[2][KW];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * kstride + (h * D + u * (D / 4)) * ESZ);
         uint4 w[KW / 4];
-        if (KW / 4 == 4) {
+        const uint4* src = reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * kstride +
+                                                          (h * D + (kInterleaved ? 0 : u * (D / 4))) * ESZ);
+        if (kInterleaved) {
+          // pieces 4c + u: the four lanes of a group read four consecutive
+          // 16-byte units, and rows 64 bytes past a multiple of 128 put the
+          // next group's row in the other half of the banks
+#pragma unroll
+          for (int c = 0; c < KW / 4; ++c) w[c] = src[4 * c + u];
+        } else if (KW / 4 == 4) {
           const int r = SP ? 0 : (u >> 1) | ((gq & 1) << 1);
 #pragma unroll
           for (int c = 0; c < 4; ++c) w[c] = src[c ^ r];
