@@ -15,7 +15,7 @@
 //                     all kv heads are contiguous inside a 64-token block),
 //                     into a ring of shared-memory stages with full/empty
 //                     mbarriers.  The V rows go in four groups of 4 tokens
-//                     placed 32 (fp8) or 64 (bf16) bytes apart, so that the
+//                     shifted by a few 16-byte units (v_row), so that the
 //                     fragment loads below spread over the banks.
 //   warps 0..Hkv-1    warp h serves kv head h and its G <= 8 query heads, on
 //                     the tensor cores (warp-level mma.sync m16n8k16, f32
@@ -128,7 +128,8 @@ __device__ __forceinline__ int v_row(int t, int kbytes, int row_bytes) {
 }
 
 template <int D, int G, bool F8, bool SP>
-__global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ? 2 : 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int ESZ = F8 ? 1 : 2;  // cache bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
   const int hkv = p.kv_heads;
@@ -199,15 +200,15 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
 
   if (SP && warp >= hkv) {
     // ------------------------------------------------------ gather warps
-    // The gather warps share a step's 32 copies, the K row (c < 16) and the
-    // V row (c >= 16) of each of its 16 listed keys: copy c is issued by lane
-    // c / NG of gather warp c % NG.  The rows of the list
-    // entries are resolved ahead, a group of 8 steps (128 entries) at a time
-    // (lane l holds entries l + 32 j of a group): while group g is copied,
-    // the block-table entries of group g + 1 and the list entries of group
-    // g + 2 are in flight, so that these dependent loads stay off the copy
-    // path.  Every gather warp resolves the rows itself and arrives on the
-    // stage's full barrier with its own bytes.
+    // The NG gather warps share a step's 32 copies, the K row (c < 16) and
+    // the V row (c >= 16) of each of its 16 listed keys: copy c is issued by
+    // lane c / NG of gather warp c % NG.  The rows of the list entries are
+    // resolved ahead, a group of 8 steps (128 entries) at a time (lane l
+    // holds entries l + 32 j of a group): while group g is copied, the
+    // block-table entries of group g + 1 and the list entries of group g + 2
+    // are in flight, so that these dependent loads stay off the copy path.
+    // Every gather warp resolves the rows itself and arrives on the stage's
+    // full barrier with its own bytes.
     const int gw = warp - hkv;
     constexpr int NG = gather_warps<F8>();
     const int c = gw + NG * lane;  // this lane's copy (c < 32)
@@ -359,7 +360,9 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     // thread in the group.
     //   S^T[16 tokens x 8 heads] = K[16 x D] Q^T[D x 8]: k-step s, logical
     //     k = 2u + b + 8c maps to dim u D/4 + 4s + 2c + b, so a thread's
-    //     codes of one token are D/4 consecutive bytes.
+    //     codes of one token are D/4 consecutive ones.  (bf16 top-k: the
+    //     same D/4 positions are taken from the 8-dim pieces 4c' + u, for
+    //     q and K alike.)
     //   O^T[D x 8 heads] += V^T[D x 16 tokens] P^T[16 x 8]: tile i, row g
     //     is dim g D/8 + 2i, row g + 8 is dim g D/8 + 2i + 1; logical
     //     k = 2u + b + 8c maps to token 4u + b + 2c, so a thread reads D/8
