@@ -101,7 +101,8 @@ def test_chunk_attention_small(case):
     run_and_check(q, k, v, P, C, paged, seed=P + C)
 
 
-def test_north_star_form_contiguous():
+def test_plain_entry_point_contiguous_cache():
+    """vpp_chunk_attn: contiguous cache, d_qk = d_v, bf16, default scale."""
     Hq, Hkv, d, P, C = 8, 2, 128, 300, 260
     q, k, v = make_seq(P + C, Hq, Hkv, d, d, seed=41)
     kc = k.to(DEV).contiguous()
