@@ -61,7 +61,7 @@ constexpr int kStepTokens = 16;
 template <bool F8> constexpr int gather_warps() { return F8 ? 2 : 4; }
 // Stage ring: six fp8 stages (32 rows of 1 KB + group and row padding) or
 // three bf16 stages of 64 KB, for 8 kv heads of d 128.
-constexpr int kDecodeRing = 6 * (32 * 1024 + 576);
+constexpr int kDecodeRing = 6 * (32 * 1024 + 640);
 // fp8: half the ring, three stages, so that two CTAs share an SM: decode rows
 // measured 6% faster, and top-k gathers 1.2-1.5x faster, than with one CTA and
 // six stages.  (bf16 stages are 64 KB: one CTA per SM.)
@@ -121,10 +121,21 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // tokens, one from each group; with the shifts (fp8: 0, 32, 64, 96 bytes;
 // bf16: 0, 16, 64, 80 bytes, whose lanes read 32 bytes in two 16-byte loads)
 // the eight lanes of each quarter warp hit eight different bank groups.
-template <bool F8>
+// Top-k (SP): a lane of the group reads tokens 2u, 2u + 1, 2u + 8, 2u + 9
+// instead, so the shift follows the token pair (t / 2) mod 4, and the second
+// eight rows move 128 bytes further so that no row overlaps the next.
+template <bool F8, bool SP>
 __device__ __forceinline__ int v_row(int t, int kbytes, int row_bytes) {
-  const int g = t >> 2;
-  return kbytes + t * row_bytes + (F8 ? 32 * g : 16 * (g & 1) + 64 * (g >> 1));
+  const int g = SP ? (t >> 1) & 3 : t >> 2;
+  return kbytes + t * row_bytes + (F8 ? 32 * g : 16 * (g & 1) + 64 * (g >> 1)) + (SP ? 128 * (t >> 3) : 0);
+}
+
+// Transposes an 8x8 matrix of 16-bit values held one row pair per lane
+// (lane 4 r + c: row r, columns 2c and 2c + 1).
+__device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 template <int D, int G, bool F8, bool SP>
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   // a fragment load in different banks (see the K reads).
   const int kstride = SP ? row_bytes + (F8 ? 16 : 64) : row_bytes;
   const int kbytes = kStepTokens * kstride;
-  const int stage_bytes = kbytes + kStepTokens * row_bytes + 128;
+  const int stage_bytes = kbytes + kStepTokens * row_bytes + 256;
   constexpr int kRing = ring_bytes<F8>();
   const int nstage = min(8, kRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kRing);  // [hkv][16][G]
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
         ok = false;
         break;
       }
-      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8>(t, kbytes, row_bytes) : t * kstride);
+      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8, true>(t, kbytes, row_bytes) : t * kstride);
       if (mine_in && !valid) {  // zero-filled, so that P = 0 times it stays 0
         for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();  // before later bulk copies into these bytes
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
           bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
           const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
           for (int g4 = 0; 4 * g4 < nt; ++g4)
-            bulk_g2s(dst + v_row<F8>(4 * g4, kbytes, row_bytes), vsrc + 4 * g4 * row_bytes,
+            bulk_g2s(dst + v_row<F8, false>(4 * g4, kbytes, row_bytes), vsrc + 4 * g4 * row_bytes,
                      static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
         } else {
           mbar_arrive(full);  // invalid block: the step's rows are skipped
@@ -366,7 +377,10 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     //   O^T[D x 8 heads] += V^T[D x 16 tokens] P^T[16 x 8]: tile i, row g
     //     is dim g D/8 + 2i, row g + 8 is dim g D/8 + 2i + 1; logical
     //     k = 2u + b + 8c maps to token 4u + b + 2c, so a thread reads D/8
-    //     consecutive codes of each token of V group u.
+    //     consecutive codes of each token of V group u, and P goes through
+    //     shared memory.  (Top-k: k maps to token k itself, so P^T's
+    //     fragment is P's accumulator fragment transposed in registers, and
+    //     a thread reads tokens 2u, 2u + 1, 2u + 8, 2u + 9.)
     // Heads >= G are zero columns.  E4M3 codes widen exactly to f16; q is
     // scaled by a power of two per head into f16's range (undone on the
     // scores), P is in [0, 256].
@@ -523,6 +537,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
           sc[rr][hh] = (tv && 2 * u + hh < G) ? (sa[0][2 * rr + hh] + sa[1][2 * rr + hh]) * slh[hh] : -INFINITY;
       }
       // ---- online softmax per head (the 8 lanes of one u hold its 16 tokens)
+      float pvr[2][2];  // top-k: P of tokens gq, gq + 8 for heads 2u, 2u + 1
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float mx = fmaxf(sc[0][hh], sc[1][hh]);
@@ -543,22 +558,35 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
         for (int rr = 0; rr < 2; ++rr) {
           const float pv = (m[hh] == -INFINITY) ? 0.f : ex2_approx(sc[rr][hh] - m[hh]);
           lpart[hh] += pv;
-          pw[(gq + 8 * rr) * 8 + 2 * u + hh] = pv;
+          if (SP) {
+            pvr[rr][hh] = pv;
+          } else {
+            pw[(gq + 8 * rr) * 8 + 2 * u + hh] = pv;
+          }
         }
       }
-      __syncwarp();
       // ---- O^T += V^T P^T
-      const uint32_t pb0 = F8 ? pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq])
-                              : pack_bf16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
-      const uint32_t pb1 = F8 ? pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq])
-                              : pack_bf16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
-      // tokens 4u .. 4u + 3 (V group u): this thread's D/8 elements of each
+      uint32_t pb0, pb1;
+      if (SP) {
+        // P^T's B fragment is the transpose of P in the accumulator layout:
+        // tokens 2u, 2u + 1 (and + 8) of head gq after one 8x8 transpose each
+        pb0 = transpose8x8_b16(F8 ? pack_f16x2(pvr[0][0], pvr[0][1]) : pack_bf16x2(pvr[0][0], pvr[0][1]));
+        pb1 = transpose8x8_b16(F8 ? pack_f16x2(pvr[1][0], pvr[1][1]) : pack_bf16x2(pvr[1][0], pvr[1][1]));
+      } else {
+        __syncwarp();
+        pb0 = F8 ? pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq])
+                 : pack_bf16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
+        pb1 = F8 ? pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq])
+                 : pack_bf16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
+      }
+      // tokens 4u .. 4u + 3 (top-k: 2u, 2u + 1, 2u + 8, 2u + 9): this
+      // thread's D/8 elements of each
       constexpr int VW = D * ESZ / 32;  // 32-bit words of them
       uint32_t vw[4][VW];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int t = 4 * u + q4;
-        const uint8_t* src = kst + v_row<F8>(t, kbytes, row_bytes) + (h * D + gq * (D / 8)) * ESZ;
+        const int t = SP ? 2 * u + (q4 & 1) + 8 * (q4 >> 1) : 4 * u + q4;
+        const uint8_t* src = kst + v_row<F8, SP>(t, kbytes, row_bytes) + (h * D + gq * (D / 8)) * ESZ;
         uint32_t w[VW];
         if (VW == 8) {
           const uint4 w0 = reinterpret_cast<const uint4*>(src)[0];
