@@ -125,10 +125,29 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // instead, so the shift follows the token pair (t / 2) mod 4, and the second
 // eight rows move 128 bytes further so that no row overlaps the next.
 template <bool F8, bool SP>
-__device__ __forceinline__ int v_row(int t, int kbytes, int row_bytes) {
+__host__ __device__ constexpr int v_row(int t, int kbytes, int row_bytes) {
   const int g = SP ? (t >> 1) & 3 : t >> 2;
   return kbytes + t * row_bytes + (F8 ? 32 * g : 16 * (g & 1) + 64 * (g >> 1)) + (SP ? 128 * (t >> 3) : 0);
 }
+// The V area of a stage: 16 rows plus at most 256 bytes of shifts.
+constexpr int kVShiftBytes = 256;
+
+// Every V row of a stage is 16-byte aligned, ends before the next begins and
+// inside the V area, for every row size the kernels use (a multiple of 64).
+template <bool F8, bool SP>
+constexpr bool v_rows_ok() {
+  for (int rb = 64; rb <= 8 * 128 * (F8 ? 1 : 2); rb += 64) {
+    for (int t = 0; t < kStepTokens; ++t) {
+      const int a = v_row<F8, SP>(t, 0, rb);
+      const int next = t + 1 < kStepTokens ? v_row<F8, SP>(t + 1, 0, rb) : kStepTokens * rb + kVShiftBytes;
+      if (a % 16 != 0 || a + rb > next) return false;
+    }
+  }
+  return true;
+}
+static_assert(v_rows_ok<false, false>() && v_rows_ok<false, true>() && v_rows_ok<true, false>() &&
+                  v_rows_ok<true, true>(),
+              "V rows of a stage overlap or leave the stage");
 
 // Transposes an 8x8 matrix of 16-bit values held one row pair per lane
 // (lane 4 r + c: row r, columns 2c and 2c + 1).
@@ -153,7 +172,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   // a fragment load in different banks (see the K reads).
   const int kstride = SP ? row_bytes + (F8 ? 16 : 64) : row_bytes;
   const int kbytes = kStepTokens * kstride;
-  const int stage_bytes = kbytes + kStepTokens * row_bytes + 256;
+  const int stage_bytes = kbytes + kStepTokens * row_bytes + kVShiftBytes;
   constexpr int kRing = ring_bytes<F8>();
   const int nstage = min(8, kRing / stage_bytes);
   float* pbuf = reinterpret_cast<float*>(smem + kRing);  // [hkv][16][G]
