@@ -677,14 +677,14 @@ def schedule_summary(tau_ms):
 EX2_PER_CLK_PER_SM = 32
 
 
-def ex2_bound(w, chunks, attn_ms_step, clk, dev):
+def ex2_bound(w, chunks, attn_ms_step, clk, sms):
     """The secondary bound of the softmax: one exp2 per unmasked score per
-    head, at the MUFU rate, against the step's attention time."""
+    head, at the MUFU rate of `sms` SMs at the sampled clock, against the
+    step's attention time."""
     exps = sum(w.heads * (C * P + C * (C + 1) // 2) for P, C in chunks)
     mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz")
     if not mhz:
         return None
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ms = exps / (EX2_PER_CLK_PER_SM * sms * mhz * 1e6) * 1e3
     return {"exps_per_step": exps, "per_clk_per_sm": EX2_PER_CLK_PER_SM, "sm_mhz": mhz, "ms": round(ms, 3),
             "frac_of_attention_time": round(ms / attn_ms_step, 4)}
@@ -913,7 +913,8 @@ def run_ours(args, dist_):
             "per_chunk": per_chunk,
             "late_chunks_tflops": round(late_tf, 1),
             "late_chunks_frac_peak": round(late_tf / peak_tf, 4),
-            "ex2_bound": ex2_bound(w, chunks, attn_ms_step, clk, dev),
+            "ex2_bound": ex2_bound(w, chunks, attn_ms_step, clk,
+                                   torch.cuda.get_device_properties(dev).multi_processor_count),
             "latency_fit_vs_k": fit,
             "schedule": schedule_summary(per_chunk_ms) if len(per_chunk_ms) > 1 else None,
             "prefill_tokens_per_s": round(w.seq_len / (attn_ms_step / 1e3), 1),
