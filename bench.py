@@ -39,8 +39,8 @@ from chunked_prefill_causal_gb300 import workloads as W  # noqa: E402
 METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens/s"
 
 # DRAM bytes (read + write) per launch of the chunk-attention kernel, averaged
-# over the 8 launches of one long128k step, from one ncu capture
-# (profiles/chunk_attn_long128k.md).  Valid only for the kernel sources whose
+# over the 8 launches of one long128k step, from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum.  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
 TRAFFIC = {"long128k": {"sources_sha256": "4df847925765ffcfbcbe519982cc19d44ceb1b92909134e7244b1b1ada6ccc09", "bytes_per_launch": 1.223e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]

@@ -44,8 +44,8 @@ def build(verbose: bool = False, jobs: int | None = None, extra_flags=(), out_di
     """Compiles what changed and (re)links the library; returns its path.
 
     The default is the product library, _build/libvpp.so.  A different
-    out_dir with extra_flags builds a variant beside it (the timeline build
-    of timeline.py) without touching the product's objects."""
+    out_dir with extra_flags builds a variant beside it (for example a
+    tracing build) without touching the product's objects."""
     out = out_dir or OUT_DIR
     lib = os.path.join(out, lib_name)
     os.makedirs(out, exist_ok=True)

@@ -24,7 +24,7 @@ Sources (cited by page title, section and equation):
   - section "预备知识：分块与三种气泡": a mixed micro-batch holds prefill
     chunks (many tokens per request) and decode requests (one token each).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * d in Eq. (1) is the per-head query/key dimension: scale = 1/sqrt(head_dim_qk).
 * Query i of a chunk with prefix P sits at absolute position P + i and attends

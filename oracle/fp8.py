@@ -16,7 +16,7 @@ Sources:
   field 0 holds subnormals (m / 8) * 2^-6; there are no infinities; S.1111.111
   is NaN, so the largest finite magnitude is S.1111.110 = 448.
 
-Readings (listed in DESIGN.md):
+Readings:
 
 * One float32 scale per kv head for K and one for V; an element's value is
   decode(code) * scale.

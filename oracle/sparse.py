@@ -16,7 +16,7 @@ Sources:
   some layers reuse another layer's indices), and the main attention reads
   only those tokens.
 
-Readings (listed in the design doc): query token i of a chunk, at absolute
+Readings: query token i of a chunk, at absolute
 position P + i, attends exactly the key positions listed in its index row,
 idx[i, :len[i]], each in 0 .. P + i; the same row serves every head (one
 index set per token, as with a single latent KV head); within the row the
