@@ -22,7 +22,10 @@
 //               as tiles are released.
 //   warp 1, 3   MMA issuers, one elected lane each: warp 1 for query tile A,
 //               warp 3 for tile B.  S = Q K^T into TMEM (kind::f16, bf16 in,
-//               f32 accumulate), then O += P V with P read from TMEM.  Each
+//               f32 accumulate), then O += P V with P read from TMEM (for
+//               d_qk <= 128 as two chains: keys [0, 64) as soon as the
+//               softmax has stored their P, keys [64, 128) once the rest is
+//               stored).  Each
 //               issuer emits blocks [PV(x, j-1), QK(x, j)] and the two take
 //               turns (a shared counter, handed over four MMAs before the end
 //               of a block), so the tensor core runs A's block j, B's block j,
@@ -35,7 +38,9 @@
 //   warp 2      allocates and frees the 512 TMEM columns.
 //   warps 4-7   softmax + epilogue of query tile A; warps 8-11 of tile B.
 //               Each thread owns one query row = one TMEM lane, so row max and
-//               row sum need no shuffles.
+//               row sum need no shuffles.  The TMA/MMA warpgroup runs on 64
+//               registers per thread so that the softmax threads get 216 and
+//               hold a whole 128-score row without spilling.
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+DV) O_B [256+DV,256+2DV).
 // P (bf16 pairs) overwrites the first 64 columns of its S tile.
 //
@@ -48,12 +53,14 @@
 // status word and every role leaves its loop.
 #pragma once
 
+#include <type_traits>
+
 #include "chunk_attn.cuh"
 #include "ptx.cuh"
 
 namespace vpp {
 
-// Timeline build only (-DVPP_TIMELINE=<cta>, see timeline.py): clock64 stamps
+// Tracing build only (compiled with -DVPP_TIMELINE=<cta>): clock64 stamps
 // of the two MMA issuers and of the first softmax thread of each query tile,
 // for CTA 0 and CTA <cta>, tiles 0..63.  The product build compiles them out.
 #ifdef VPP_TIMELINE
@@ -71,8 +78,8 @@ namespace attn_detail {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
-constexpr int kRegsLow = 112;
-constexpr int kRegsHigh = 192;
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch");
 constexpr uint64_t kCleanupNs = 100000000ull;  // 0.1 s for clean-up waits after an abort
 
@@ -97,9 +104,18 @@ struct Shape {
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kTileN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, DV, false, true);
   static constexpr uint32_t IDESC_PV64 = idesc_bf16_f32(kTileM, 64, false, true);
-  // barrier indices: Q, S[2], P[2], O[2], FINAL[2], TMP, FULL[NB], EMPTY[NB]
-  static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_FULL = 10,
-                       B_EMPTY = 10 + NB, NBARS = 10 + 2 * NB;
+  // P V of a tile runs as two MMA chains over 16-key steps: the first covers
+  // keys [0, 16 * PV0) and starts once the softmax has stored their P, while
+  // the softmax still computes the exponentials of the remaining keys.  With
+  // d_qk = 192 the split measured slower (the ring, not the softmax, limits
+  // that shape), so it keeps one chain.
+  static constexpr int PV0 = DQ > 128 ? 8 : 4;
+  static constexpr int KP0 = 16 * PV0;  // keys of the first part
+  static constexpr bool SPLIT_P = PV0 < kTileN / 16;  // PV0 = 8: one chain
+  static_assert(PV0 >= 1 && PV0 <= kTileN / 16, "P V chain split out of range");
+  // barrier indices: Q, S[2], P0[2], O[2], FINAL[2], TMP, P1[2], FULL[NB], EMPTY[NB]
+  static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_P1 = 10,
+                       B_FULL = 12, B_EMPTY = 12 + NB, NBARS = 12 + 2 * NB;
   static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
   // With d_qk = 192 the ring holds under two K/V tile pairs, and the next K
   // tile can only start once V_{j-1} is free: V_{j-1} is released by its own
@@ -120,6 +136,30 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* st
                                           volatile uint32_t* abort) {
   const bool ok = mbar_wait(bar, parity, status, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// p = 2^(s * scale * log2(e) - mref) for the scores of keys [K0, K1) of a
+// row, two lanes of work per packed instruction, stored to TMEM as bf16 pairs
+// (column c of the tile holds keys 2c, 2c + 1) every 16 keys, so that packed
+// values do not pile up in registers; the fp32 values are added to rs4.
+template <int K0, int K1>
+__device__ __forceinline__ void exps_to_tmem(const float (&sv)[128], float2 sl2, float2 nmb2,
+                                             float2 (&rs4)[4], uint32_t tS) {
+  static_assert(K0 % 16 == 0 && K1 % 16 == 0, "parts are whole 16-key MMA steps");
+#pragma unroll
+  for (int k = K0 / 16; k < K1 / 16; ++k) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 8 * k + i;  // pair index
+      const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
+      const float a = ex2_approx(xx.x);
+      const float b = ex2_approx(xx.y);
+      rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
+      pk[i] = pack_bf16x2(a, b);
+    }
+    tmem_st8(tS + 8 * k, pk);
+  }
 }
 
 }  // namespace attn_detail
@@ -174,6 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(S::B_S + x), 1);
       mbar_init(bar(S::B_P + x), 128);
+      mbar_init(bar(S::B_P1 + x), 128);
       mbar_init(bar(S::B_O + x), 1);
       mbar_init(bar(S::B_FINAL + x), 1);
     }
@@ -330,7 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!(ok = mbar_wait(bar(S::B_FULL + tv % S::NB), (tv / S::NB) & 1u, p.status, abort_flag))) break;
           if (!(ok = mbar_wait(bar(S::B_P + x), (j - 1) & 1, p.status, abort_flag))) break;
           tc_fence_after();
-          VPP_STAMP(x, j, 0);  // P of tile j-1 seen
+          VPP_STAMP(x, j, 0);  // first part of P of tile j-1 seen
         }
         if (j < n_kv &&
             !(ok = mbar_wait(bar(S::B_FULL + tk % S::NB), (tk / S::NB) & 1u, p.status, abort_flag)))
@@ -355,28 +396,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         VPP_STAMP(x, j, 1);  // turn taken
         if (j > 0) {
-          // O += P V for tile j-1 (P read from TMEM, V from the ring).
-          if (S::NVC == 1 || vslot + S::NVC <= S::NSLOT) {
-            // Adjacent V sub-tiles: one N = DV chain (LBO = one sub-tile).
-            const uint64_t vb = dv0 + vslot * kSub16;
+          // O += P V for tile j-1 (P read from TMEM, V from the ring), as two
+          // chains of 16-key steps: [0, PV0) now, [PV0, 8) once the softmax
+          // has stored the rest of P.
+          const bool adjacent = S::NVC == 1 || vslot + S::NVC <= S::NSLOT;
+          auto pv_steps = [&](int k0, int k1) {
+            if (adjacent) {
+              // Adjacent V sub-tiles: one N = DV chain (LBO = one sub-tile).
+              const uint64_t vb = dv0 + vslot * kSub16;
 #pragma unroll
-            for (int k = 0; k < kTileN / 16; ++k)
-              umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 1 || k > 0) ? 1u : 0u);
-          } else {
-            // The V tile wraps around the ring: one N = 64 chain per sub-tile.
+              for (int k = k0; k < k1; ++k)
+                umma_ts(tO, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV, (j > 1 || k > 0) ? 1u : 0u);
+            } else {
+              // The V tile wraps around the ring: one N = 64 chain per sub-tile.
 #pragma unroll
-            for (int h = 0; h < S::NVC; ++h) {
-              const int vs = vslot + h < S::NSLOT ? vslot + h : vslot + h - S::NSLOT;
-              const uint64_t vb = dv0 + vs * kSub16;
+              for (int k = k0; k < k1; ++k)
 #pragma unroll
-              for (int k = 0; k < kTileN / 16; ++k)
-                umma_ts(tO + 64 * h, tS + 8 * k, vb + k * (2048 >> 4), S::IDESC_PV64,
-                        (j > 1 || k > 0) ? 1u : 0u);
+                for (int h = 0; h < S::NVC; ++h) {
+                  const int vs = vslot + h < S::NSLOT ? vslot + h : vslot + h - S::NSLOT;
+                  umma_ts(tO + 64 * h, tS + 8 * k, dv0 + vs * kSub16 + k * (2048 >> 4), S::IDESC_PV64,
+                          (j > 1 || k > 0) ? 1u : 0u);
+                }
             }
+          };
+          pv_steps(0, S::PV0);
+          if (S::SPLIT_P) {
+            if (!(ok = mbar_wait(bar(S::B_P1 + x), (j - 1) & 1, p.status, abort_flag))) break;
+            tc_fence_after();
+            VPP_STAMP(x, j, 3);  // second part of P of tile j-1 seen
+            pv_steps(S::PV0, kTileN / 16);
           }
           if (S::EARLY_V) umma_commit(bar(S::B_EMPTY + tv % S::NB));
         }
-        VPP_STAMP(x, j, 3);  // P V issued
         if (j < n_kv) {
           // S = Q K^T for tile j; follows PV(x, j-1), which read P from the
           // same TMEM columns, in issue order.  The turn goes to the partner
@@ -463,49 +514,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                      fmaxf(mx8[6], mx8[7]));
       };
-      // p = 2^(s * scale * log2(e) - mref), two lanes of work per packed FMA,
-      // stored to TMEM in two halves (the first store overlaps the second
-      // half's exponentials); returns the row sum of p.
-      auto exps_to_tmem = [&](float mref) -> float {
+      // Exponentials of the tile's two key parts: the first part's P is stored
+      // and signalled before the second part is computed, so that the first
+      // P V chain runs meanwhile.
+      const float2 sl2 = make_float2(sl, sl);
+      float2 rs4[4];
+      auto part = [&](auto k0, auto k1, float mref) {
         const float mb = (mref == -INFINITY) ? 0.f : mref;
-        const float2 sl2 = make_float2(sl, sl);
         const float2 nmb2 = make_float2(-mb, -mb);
-        float2 rs4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
-        uint32_t pk0[32], pk1[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 xx = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2, nmb2);
-          const float a = ex2_approx(xx.x);
-          const float b = ex2_approx(xx.y);
-          rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
-          pk0[c] = pack_bf16x2(a, b);
-        }
-        tmem_st32(tS, pk0);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 xx = ffma2(make_float2(sv[64 + 2 * c], sv[64 + 2 * c + 1]), sl2, nmb2);
-          const float a = ex2_approx(xx.x);
-          const float b = ex2_approx(xx.y);
-          rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
-          pk1[c] = pack_bf16x2(a, b);
-        }
-        tmem_st32(tS + 32, pk1);
-        const float2 rs2 = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
-        return rs2.x + rs2.y;
+        exps_to_tmem<decltype(k0)::value, decltype(k1)::value>(sv, sl2, nmb2, rs4, tS);
       };
-      float rs;
+      using K_0 = std::integral_constant<int, 0>;
+      using K_P0 = std::integral_constant<int, S::KP0>;
+      using K_N = std::integral_constant<int, kTileN>;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
       if (j == 0) {
         m = row_max() * sl;
-        rs = exps_to_tmem(m);
+        part(K_0{}, K_P0{}, m);
       } else {
-        // The exponentials use the running max right away and the row max is
-        // computed alongside, off the critical path.  Only when it has grown
-        // by more than 2^8 are O and the denominator rescaled and the
-        // exponentials redone (rare after the first tile; the result is exact
-        // either way since numerator and denominator share the reference m).
-        rs = exps_to_tmem(m);
+        // The first part's exponentials use the running max right away and
+        // the row max of the whole tile is computed alongside.  Only when it
+        // has grown by more than 2^8 are O and the denominator rescaled and
+        // the first part redone, before the first part is released (rare
+        // after the first tile; the result is exact either way since
+        // numerator and denominator share the reference m).
+        part(K_0{}, K_P0{}, m);
         const float m_new = fmaxf(m, row_max() * sl);
         const bool need = m_new > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
@@ -526,15 +560,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             tmem_st32(tO + 32 * q, o);
           }
-          tmem_st_wait();
-          rs = exps_to_tmem(m);  // rows whose m did not move rewrite the same values
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rs4[i] = make_float2(0.f, 0.f);
+          part(K_0{}, K_P0{}, m);  // rows whose m did not move recompute the same values
         }
       }
-      if (row == 0) VPP_STAMP(2 + x, j, 2);  // exponentials done
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(S::B_P + x));
-      if (row == 0) VPP_STAMP(2 + x, j, 3);  // P stored and signalled
+      if (row == 0) VPP_STAMP(2 + x, j, 2);  // first part of P stored and signalled
+      if (S::SPLIT_P) {
+        part(K_P0{}, K_N{}, m);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(S::B_P1 + x));
+        if (row == 0) VPP_STAMP(2 + x, j, 3);  // second part of P stored and signalled
+      }
+      const float2 rs2 = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
+      const float rs = rs2.x + rs2.y;
       l += rs;
     }
     if (ok) ok = warp_wait(bar(S::B_O + x), 0, p.status, abort_flag);

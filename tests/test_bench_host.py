@@ -29,3 +29,35 @@ def test_recorded_traffic_is_null_once_the_kernel_sources_change(monkeypatch):
     assert bench.recorded_traffic("gqa32k") is None
     monkeypatch.setattr(bench, "TRAFFIC", {"long128k": {"sources_sha256": "0" * 64, "bytes_per_launch": 1.5e9}})
     assert bench.recorded_traffic("long128k") is None
+
+
+def test_mixed_launch_count_and_combined_bound():
+    # varlen append + decode kernel + its merge + one chunk-attention launch per 64 segments
+    assert bench.mixed_launches(4, 256) == 4
+    assert bench.mixed_launches(0, 256) == 3
+    assert bench.mixed_launches(4, 0) == 2
+    assert bench.mixed_launches(65, 1) == 5
+    # the longer of the prefill FLOPs at the tensor peak and the decode bytes at HBM bandwidth
+    assert abs(bench.mixed_bound_ms(7.0e12, 18.5e9, 1750.0, 6700.0) - 4.0) < 1e-9
+    assert abs(bench.mixed_bound_ms(1.0e12, 67.0e9, 1000.0, 6700.0) - 10.0) < 1e-9
+
+
+def test_summary_keeps_the_judged_figures_in_a_short_tail():
+    line = {"config": {"workload": "long128k"}, "value": 1500.0,
+            "roofline": {"frac": 0.86, "frac_of_burst": 0.78},
+            "late_chunks_frac_peak": 0.87, "late_chunks_tflops": 1520.0,
+            "per_chunk": [{"k": k, "ms": 3.0 + 6 * k, "tflops": 1400.0 + k, "frac_peak": 0.8} for k in range(8)],
+            "gqa32k": {"tflops": 1300.0, "frac": 0.75, "rows": [[k, 4096 * k, 4096, 1.0, 1300.0, 0.75, 0.68]
+                                                                  for k in range(8)]},
+            "mla512k": {"tflops": 1280.0, "frac": 0.74, "rows": [[k, 24576 * k, 24576, 100.0, 1280.0, 0.74, 0.66]
+                                                                   for k in (0, 10, 20, 21)]},
+            "kv_append": {"frac_hbm": 0.99},
+            "mixed": {"decode_frac_hbm": 1.07, "step_ms": 7.4, "bound_ms": 4.03, "frac_of_bound": 0.5446},
+            "cpu_baseline": {"value": 4.2e-2, "cores": 16}}
+    s = bench.summary(line, 1924.4)
+    assert s["late_frac"] == 0.87 and s["late_frac_burst"] == round(1520.0 / 1924.4, 4)
+    assert [r[0] for r in s["k_ms_tflops_frac"]] == list(range(8))
+    assert [r[0] for r in s["mla512k"]["k_ms_tflops_frac"]] == [0, 10, 20, 21]
+    assert s["mixed_frac_of_bound"] == 0.5446 and s["append_frac_hbm"] == 0.99
+    import json
+    assert len(json.dumps(s)) < 1400
