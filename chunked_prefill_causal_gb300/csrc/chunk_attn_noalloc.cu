@@ -36,20 +36,41 @@ std::mutex g_scratch_mutex;
 void* g_scratch_ptr[64] = {};
 
 // Device address of the scratch array on the current device (set-up once per
-// device, under a lock).
+// device, under a lock).  The library's kernels are built for compute
+// capability 10.3 only, so any other device is refused before the lookup; a
+// failed lookup clears the runtime's error state so that the caller's next
+// cudaGetLastError does not report it a second time.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return VPP_ERR_CUDA;
   if (dev < 0 || dev >= 64) return VPP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
       return VPP_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return VPP_ERR_UNSUPPORTED;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return VPP_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = ptr;
   }
   *out = g_scratch_ptr[dev];
   return VPP_OK;
+}
+
+// Scratch bytes that a call with this split request needs (q is bf16, so only
+// the split partials), or a negative status.
+int64_t scratch_need(int64_t P, int64_t C, int heads, int kv_heads, int dq, int dv, int splits) {
+  const int s = vpp_chunk_attn_num_splits(P, C, heads, kv_heads, dq, dv, splits);
+  if (s < 0) return s;
+  return static_cast<int64_t>(
+      vpp_chunk_attn_workspace_size(VPP_BF16, P, C, heads, kv_heads, dq, dv, splits));
 }
 
 }  // namespace
@@ -62,13 +83,24 @@ extern "C" int vpp_chunk_attn_noalloc(const void* q, const void* k_cache, const 
                                       void* stream) {
   if (prefix_len < 0 || chunk_len < 0 || num_splits < 0) return VPP_ERR_INVALID;
   if (chunk_len == 0) return VPP_OK;
-  // Scratch this call needs (split partials; q is bf16, so nothing else).
-  const int s = vpp_chunk_attn_num_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
-                                          head_dim_v, num_splits);
-  if (s < 0) return s;
-  const size_t need = vpp_chunk_attn_workspace_size(VPP_BF16, prefix_len, chunk_len, heads,
-                                                    kv_heads, head_dim_qk, head_dim_v, num_splits);
-  if (need > kNoallocScratchBytes) return VPP_ERR_WORKSPACE;
+  int64_t need = scratch_need(prefix_len, chunk_len, heads, kv_heads, head_dim_qk, head_dim_v,
+                              num_splits);
+  if (need < 0) return static_cast<int>(need);
+  if (num_splits == 0 && need > static_cast<int64_t>(kNoallocScratchBytes)) {
+    // The library's own choice of key ranges does not fit the array: take the
+    // largest explicit count whose partials do (one range needs none).
+    int s = vpp_chunk_attn_num_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
+                                      head_dim_v, 0);
+    while (s > 1) {
+      --s;
+      need = scratch_need(prefix_len, chunk_len, heads, kv_heads, head_dim_qk, head_dim_v, s);
+      if (need < 0) return static_cast<int>(need);
+      if (need <= static_cast<int64_t>(kNoallocScratchBytes)) break;
+    }
+    num_splits = s;
+    if (s == 1) need = 0;
+  }
+  if (need > static_cast<int64_t>(kNoallocScratchBytes)) return VPP_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
     if (int r = scratch_address(&scratch)) return r;

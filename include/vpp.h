@@ -153,10 +153,14 @@ int vpp_chunk_attn_ex(const void *q, int q_dtype, const void *k_cache,
  * Same arguments and results as vpp_chunk_attn_ex with q_dtype = VPP_BF16 and
  * no workspace.  When the key range is split, the float32 partials live in a
  * fixed 32 MiB array in device memory that the library holds on every GPU
- * that loads it, until the process exits.  Calls whose partials would exceed
- * 32 MiB (num_splits x chunk_len x heads x (head_dim_v + 1) x 4 bytes, see
- * vpp_chunk_attn_workspace_size) return VPP_ERR_WORKSPACE and launch nothing.
- * The first call on a device looks up that array's device address (with the
+ * that loads it, until the process exits.  The partials take about
+ * num_splits x chunk_len x heads x (head_dim_v + 1) x 4 bytes (exactly
+ * vpp_chunk_attn_workspace_size for the same arguments).  With num_splits = 0
+ * the library lowers its own choice of key ranges to the largest count whose
+ * partials fit (one range needs none), so such a call always runs.  An
+ * explicit num_splits > 1 whose partials exceed 32 MiB returns
+ * VPP_ERR_WORKSPACE and launches nothing.  A device other than compute
+ * capability 10.3 gives VPP_ERR_UNSUPPORTED.  The first call on a device looks up that array's device address (with the
  * device current); make that first call before any stream capture.  All calls
  * on a device share the array and it keeps the last call's contents (nothing
  * in it needs to start at zero), so calls that overlap on the GPU race: issue

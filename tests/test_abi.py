@@ -139,3 +139,23 @@ def test_split_plan_is_host_side(lib):
     assert ws >= 4 * 64 * 8 * 128 * 4
     assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, 100000, 64, 8, 8, 128, 128, 1) == 0
     assert vpp.chunk_attn_workspace_size(vpp.VPP_FP32, 0, 64, 8, 8, 128, 128, 1) == 64 * 8 * 128 * 2
+
+
+def test_noalloc_host_checks_run_before_any_device_call(lib):
+    null = None
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced
+    f = lib.vpp_chunk_attn_noalloc
+    # an empty chunk is a no-op, even with NULL tensors
+    assert f(null, null, null, null, 1, 100, 0, 8, 2, 128, 128, ctypes.c_float(0.0), 0, null, null, null) == vpp.VPP_OK
+    # unsupported head dims and groupings
+    assert f(fake, fake, fake, null, 256, 100, 16, 8, 2, 96, 96, ctypes.c_float(0.0), 0, fake, null, null) == \
+        vpp.VPP_ERR_UNSUPPORTED
+    assert f(fake, fake, fake, null, 256, 100, 16, 8, 2, 128, 192, ctypes.c_float(0.0), 0, fake, null, null) == \
+        vpp.VPP_ERR_UNSUPPORTED
+    assert f(fake, fake, fake, null, 256, 100, 16, 24, 8, 128, 128, ctypes.c_float(0.0), 0, fake, null, null) == \
+        vpp.VPP_ERR_UNSUPPORTED
+    # negative sizes and split requests
+    assert f(fake, fake, fake, null, 256, -1, 16, 8, 2, 128, 128, ctypes.c_float(0.0), 0, fake, null, null) == \
+        vpp.VPP_ERR_INVALID
+    assert f(fake, fake, fake, null, 256, 100, 16, 8, 2, 128, 128, ctypes.c_float(0.0), -1, fake, null, null) == \
+        vpp.VPP_ERR_INVALID

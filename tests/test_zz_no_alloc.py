@@ -15,26 +15,34 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from chunked_prefill_causal_gb300 import vpp
-from tests.helpers import LSE_ABS, errors, random_table, to_np64
+from tests.helpers import LSE_ABS, assert_close, errors, random_table, to_np64
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
 
-def _case(Hq, Hkv, d, P, C, seed):
+def _inputs(Hq, Hkv, d, P, C, seed):
     g = torch.Generator(device="cpu").manual_seed(seed)
     std = 1 / math.sqrt(d)
-    q = (torch.randn((C, Hq, d), generator=g) * std).to(torch.bfloat16).to(DEV)
-    k = (torch.randn((P + C, Hkv, d), generator=g) * std).to(torch.bfloat16).to(DEV)
-    v = (torch.randn((P + C, Hkv, d), generator=g) * std).to(torch.bfloat16).to(DEV)
+    q = (torch.randn((C, Hq, d), generator=g) * std).to(torch.bfloat16)
+    k = (torch.randn((P + C, Hkv, d), generator=g) * std).to(torch.bfloat16)
+    v = (torch.randn((P + C, Hkv, d), generator=g) * std).to(torch.bfloat16)
+    return q, k, v
+
+
+def _case(Hq, Hkv, d, P, C, seed, host=False):
+    q, k, v = _inputs(Hq, Hkv, d, P, C, seed)
     need = (P + C + 63) // 64
     table = torch.from_numpy(random_table(need, need + 3, seed)).to(DEV)
     kc = torch.zeros((need + 3, 64, Hkv, d), dtype=torch.bfloat16, device=DEV)
     vc = torch.zeros_like(kc)
-    vpp.vpp_kv_append(k, v, kc, vc, 0, block_table=table)
-    return q, kc, vc, table
+    vpp.vpp_kv_append(k.to(DEV), v.to(DEV), kc, vc, 0, block_table=table)
+    if host:
+        return q.to(DEV), kc, vc, table, (q, k, v)
+    return q.to(DEV), kc, vc, table
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
@@ -61,3 +69,43 @@ def test_noalloc_refuses_partials_larger_than_its_array():
     with pytest.raises(vpp.VppError) as e:
         vpp.vpp_chunk_attn_noalloc(q, kc, vc, P, block_table=table, num_splits=2)
     assert e.value.code == vpp.VPP_ERR_WORKSPACE
+
+
+def test_noalloc_matches_the_oracle_unsplit_split_and_library_chosen():
+    # One range (no scratch used), an explicit split, and the library's own
+    # choice, each against the fp64 oracle on the same inputs.
+    Hq, Hkv, d, P, C = 16, 4, 128, 1500, 300
+    q, kc, vc, table, (qh, kh, vh) = _case(Hq, Hkv, d, P, C, 21, host=True)
+    ref, ref_lse = oracle.causal_chunk_attention(to_np64(qh), to_np64(kh), to_np64(vh), P)
+    for splits in (1, 2, 0):
+        lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+        got = vpp.vpp_chunk_attn_noalloc(q, kc, vc, P, block_table=table, lse=lse, num_splits=splits)
+        torch.cuda.synchronize()
+        assert vpp.vpp_last_device_status() == 0
+        assert_close(to_np64(got), ref, what=f"noalloc num_splits={splits}")
+        assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
+
+
+def test_noalloc_lowers_the_library_split_choice_to_fit_its_array():
+    # In both shapes the library would split the prefix for speed into ranges
+    # whose partials exceed 32 MiB.  The call then takes the largest range
+    # count that fits (three ranges in the first shape, none in the second)
+    # instead of refusing, and its result is bit for bit the workspace entry
+    # point's with that count.
+    limit = 32 << 20
+    Hq, Hkv, d = 32, 8, 128
+    for P, C, expect, seed in ((40000, 512, 3, 22), (60000, 2048, 1, 23)):
+        auto = vpp.chunk_attn_num_splits(P, C, Hq, Hkv, d, d, 0)
+        assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, P, C, Hq, Hkv, d, d, 0) > limit
+        fit = max(s for s in range(1, auto + 1)
+                  if vpp.chunk_attn_workspace_size(vpp.VPP_BF16, P, C, Hq, Hkv, d, d, s) <= limit)
+        assert fit == expect
+        q, kc, vc, table = _case(Hq, Hkv, d, P, C, seed)
+        lse_a = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+        lse_b = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+        ref = vpp.vpp_chunk_attn_ex(q, kc, vc, P, block_table=table, lse=lse_a, num_splits=fit)
+        got = vpp.vpp_chunk_attn_noalloc(q, kc, vc, P, block_table=table, lse=lse_b, num_splits=0)
+        torch.cuda.synchronize()
+        assert vpp.vpp_last_device_status() == 0
+        assert torch.equal(got, ref)
+        assert torch.equal(lse_b, lse_a)
