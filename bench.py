@@ -330,6 +330,9 @@ class MixedSetup:
             need8 = vpp.mixed_attn_fp8_workspace_size(self.cu, self.ctx, m.heads, m.kv_heads, m.head_dim_qk,
                                                       m.head_dim_v)
             self.ws8 = torch.empty(max(need8, 256), dtype=torch.uint8, device=dev)
+            need8w = vpp.mixed_attn_fp8_widen_workspace_size(self.cu, self.ctx, m.heads, m.kv_heads,
+                                                             m.head_dim_qk, m.head_dim_v)
+            self.ws8w = torch.empty(max(need8w, 256), dtype=torch.uint8, device=dev)
 
     def step_fp8(self):
         from chunked_prefill_causal_gb300 import vpp
@@ -337,6 +340,15 @@ class MixedSetup:
                                      self.cu, self.ctx)
         vpp.vpp_mixed_attn_fp8(self.q, self.kc8, self.vc8, self.ks8, self.vs8, self.table, self.cu, self.ctx,
                                out=self.out, lse=self.lse, workspace=self.ws8)
+
+    def step_fp8_widened(self):
+        """As step_fp8, with a workspace that holds the bf16 widening of the
+        prefill segments' contexts."""
+        from chunked_prefill_causal_gb300 import vpp
+        vpp.vpp_kv_append_varlen_fp8(self.k_new, self.v_new, self.kc8, self.vc8, self.ks8, self.vs8, self.table,
+                                     self.cu, self.ctx)
+        vpp.vpp_mixed_attn_fp8(self.q, self.kc8, self.vc8, self.ks8, self.vs8, self.table, self.cu, self.ctx,
+                               out=self.out, lse=self.lse, workspace=self.ws8w)
 
     def decode_only_fp8(self):
         from chunked_prefill_causal_gb300 import vpp
@@ -499,12 +511,13 @@ def measure_fp8(dev, stream, hbm, w, chunks):
     dec8 = time_events(ms.decode_only_fp8, 10, stream)
     step = time_events(ms.step, 10, stream)
     step8 = time_events(ms.step_fp8, 10, stream)
+    step8w = time_events(ms.step_fp8_widened, 10, stream)
     b8 = ms.decode_bytes // 2
     out["decode"] = {"rows": len(ms.ctx_d), "bytes_fp8": int(b8), "ms_fp8": round(dec8, 3), "ms_bf16": round(dec, 3),
                      "gbs_fp8": round(b8 / (dec8 / 1e3) / 1e9, 1),
                      "frac_hbm_fp8": round(b8 / (dec8 / 1e3) / 1e9 / hbm, 4),
                      "speedup_vs_bf16": round(dec / dec8, 3)}
-    out["mixed_step"] = {"ms_fp8": round(step8, 3), "ms_bf16": round(step, 3)}
+    out["mixed_step"] = {"ms_fp8": round(step8, 3), "ms_fp8_widened": round(step8w, 3), "ms_bf16": round(step, 3)}
     del ms
     torch.cuda.empty_cache()
 
@@ -524,12 +537,18 @@ def measure_fp8(dev, stream, hbm, w, chunks):
         q = qi
         del ki, vi
     o = torch.empty((C, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
-    ws8 = torch.empty(vpp.chunk_attn_fp8_workspace_size(P, C, w.heads, w.kv_heads, w.head_dim_qk, w.head_dim_v, 1),
-                      dtype=torch.uint8, device=dev)
+    ws8 = torch.empty(max(256, vpp.chunk_attn_fp8_workspace_size(P, C, w.heads, w.kv_heads, w.head_dim_qk,
+                                                                 w.head_dim_v, 1)), dtype=torch.uint8, device=dev)
+    ws8w = torch.empty(vpp.chunk_attn_fp8_widen_workspace_size(P, C, w.heads, w.kv_heads, w.head_dim_qk,
+                                                               w.head_dim_v, 1), dtype=torch.uint8, device=dev)
     t16 = time_events(lambda: vpp.vpp_chunk_attn_ex(q, kc16, vc16, P, out=o, num_splits=1), 5, stream)
     t8 = time_events(lambda: vpp.vpp_chunk_attn_fp8(q, kc8, vc8, s, s, P, out=o, num_splits=1, workspace=ws8),
                      5, stream)
-    out["prefill_last_chunk"] = {"prefix": P, "chunk": C, "ms_fp8": round(t8, 3), "ms_bf16": round(t16, 3),
+    t8w = time_events(lambda: vpp.vpp_chunk_attn_fp8(q, kc8, vc8, s, s, P, out=o, num_splits=1, workspace=ws8w),
+                      5, stream)
+    # in the kernel (no copy of the cache) / widened once into a bf16 copy / bf16 cache
+    out["prefill_last_chunk"] = {"prefix": P, "chunk": C, "ms_fp8": round(t8, 3), "ms_fp8_widened": round(t8w, 3),
+                                 "ms_bf16": round(t16, 3), "widened_copy_bytes": int(ws8w.numel()),
                                  "fp8_overhead": round(t8 / t16 - 1.0, 4)}
     return out
 
@@ -1046,7 +1065,8 @@ def summary(line, peak_burst):
     if "fp8_kv" in line:
         f8 = line["fp8_kv"]
         out["fp8_decode_frac_hbm"] = f8["decode"]["frac_hbm_fp8"]
-        out["fp8_last_chunk_ms"] = [f8["prefill_last_chunk"]["ms_fp8"], f8["prefill_last_chunk"]["ms_bf16"]]
+        pl = f8["prefill_last_chunk"]
+        out["fp8_last_chunk_ms"] = [pl["ms_fp8"], pl.get("ms_fp8_widened"), pl["ms_bf16"]]
     if line.get("cpu_baseline"):
         out["cpu_tflops"] = r4(line["cpu_baseline"]["value"])
         out["cpu_cores"] = line["cpu_baseline"]["cores"]

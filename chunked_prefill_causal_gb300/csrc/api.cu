@@ -137,6 +137,33 @@ int make_contig_map(CUtensorMap* m, const void* cache, int64_t n_tokens, int kv_
   return encode_map(m, cache, 3, dims, strides, box);
 }
 
+// The same two cache layouts holding one-byte E4M3 codes: plain (unswizzled)
+// boxes of 64 codes x 64 tokens, which the kernel widens itself.
+int encode_map_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box) {
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims,
+                              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VPP_OK : VPP_ERR_INVALID;
+}
+
+int make_paged_map_u8(CUtensorMap* m, const void* cache, int32_t num_blocks, int kv_heads, int d) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)kv_heads, (cuuint64_t)kBlockTokens,
+                              (cuuint64_t)num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)d, (cuuint64_t)kv_heads * d,
+                                 (cuuint64_t)kBlockTokens * kv_heads * d};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBlockTokens, 1};
+  return encode_map_u8(m, cache, 4, dims, strides, box);
+}
+
+int make_contig_map_u8(CUtensorMap* m, const void* cache, int64_t n_tokens, int kv_heads, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)kv_heads, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)kv_heads * d};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlockTokens};
+  return encode_map_u8(m, cache, 3, dims, strides, box);
+}
+
 struct SplitPlan {
   int n_splits;
   int split_keys;
@@ -190,7 +217,7 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
                     const int32_t* block_table, int32_t num_blocks, int64_t P, int64_t C,
                     int heads, int kv_heads, int dq, int dv, float scale, int num_splits,
                     void* out, float* lse, void* workspace, size_t ws_bytes, cudaStream_t st,
-                    const float* k_scale = nullptr, const float* v_scale = nullptr) {
+                    const float* k_scale = nullptr, const float* v_scale = nullptr, bool f8 = false) {
   if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
   if (C == 0) return VPP_OK;  // pointers may be NULL for an empty chunk
   if (!q || !k_cache || !v_cache || !out) return VPP_ERR_INVALID;
@@ -228,12 +255,16 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_q_map(&tm_q, q_bf16, C, heads, kv_heads, dq)) return VPP_ERR_INVALID;
   if (block_table) {
-    if (make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, dq) ||
-        make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, dv))
+    if (f8 ? make_paged_map_u8(&tm_k, k_cache, num_blocks, kv_heads, dq) ||
+                 make_paged_map_u8(&tm_v, v_cache, num_blocks, kv_heads, dv)
+           : make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, dq) ||
+                 make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, dv))
       return VPP_ERR_INVALID;
   } else {
-    if (make_contig_map(&tm_k, k_cache, P + C, kv_heads, dq) ||
-        make_contig_map(&tm_v, v_cache, P + C, kv_heads, dv))
+    if (f8 ? make_contig_map_u8(&tm_k, k_cache, P + C, kv_heads, dq) ||
+                 make_contig_map_u8(&tm_v, v_cache, P + C, kv_heads, dv)
+           : make_contig_map(&tm_k, k_cache, P + C, kv_heads, dq) ||
+                 make_contig_map(&tm_v, v_cache, P + C, kv_heads, dv))
       return VPP_ERR_INVALID;
   }
 
@@ -269,7 +300,7 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   s.ws_row0 = 0;
   const int64_t grid = (int64_t)s.n_pairs * kv_heads * s.n_splits;
   if (grid > INT32_MAX) return VPP_ERR_INVALID;
-  if (launch_chunk_attn(dq, dv, tm_q, tm_k, tm_v, p, (int)grid, st) != cudaSuccess)
+  if (launch_chunk_attn(dq, dv, f8, tm_q, tm_k, tm_v, p, (int)grid, st) != cudaSuccess)
     return VPP_ERR_CUDA;
   if (sp.n_splits > 1) {
     if (launch_lse_merge(p.ws_o, p.ws_lse, 0, sp.n_splits, (int)C, 0, heads, dv,
@@ -335,9 +366,11 @@ size_t widen_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int 
 }
 
 // Mixed micro-batch over a paged cache, bf16 or (fp8) E4M3 codes with
-// per-kv-head scales.  Chunk-attention segments of an fp8 cache read the
-// bf16 widening of their contexts from the workspace; decode rows read the
-// codes directly.
+// per-kv-head scales.  Decode rows read the codes directly.  Chunk-attention
+// segments of an fp8 cache read the codes directly as well (the fp8 kernel
+// widens them in shared memory), unless the workspace also holds the bf16
+// widening of their contexts: then they are widened once into it and read by
+// the bf16 kernel, which is faster.
 int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache,
                const float* k_scale, const float* v_scale, const int32_t* block_table,
                int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t* cu_seqlens_q,
@@ -365,10 +398,10 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
   // every other sequence with queries becomes one chunk-attention segment.
   const size_t dws = decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk,
                                      head_dim_v);
+  if (dws > 0 && (!workspace || workspace_bytes < dws || !aligned16(workspace))) return VPP_ERR_WORKSPACE;
   const size_t wws =
       fp8 ? widen_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v) : 0;
-  if (dws + wws > 0 && (!workspace || workspace_bytes < dws + wws || !aligned16(workspace)))
-    return VPP_ERR_WORKSPACE;
+  const bool widen = wws > 0 && workspace && aligned16(workspace) && workspace_bytes >= dws + wws;
 
   // Segments are ordered by per-CTA work (keys per CTA) so the heaviest CTAs
   // start first.
@@ -381,7 +414,7 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
   CUtensorMap tm_q, tm_k, tm_v;
   if (make_q_map(&tm_q, q, total_q, heads, kv_heads, head_dim_qk)) return VPP_ERR_INVALID;
   int64_t kv_base[kMaxBatch];
-  if (fp8 && n > 0) {
+  if (widen) {
     static WidenPlan zero_wplan;
     WidenPlan wp = zero_wplan;
     wp.n = n;
@@ -404,8 +437,10 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
     if (launch_kv_widen_fp8(k_cache, v_cache, k16, v16, kv_heads, head_dim_qk, head_dim_v, block_table,
                             num_blocks, wp, ds->status, ds->num_sms, st) != cudaSuccess)
       return VPP_ERR_CUDA;
-  } else if (make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
-             make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v)) {
+  } else if (fp8 ? make_paged_map_u8(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
+                       make_paged_map_u8(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v)
+                 : make_paged_map(&tm_k, k_cache, num_blocks, kv_heads, head_dim_qk) ||
+                       make_paged_map(&tm_v, v_cache, num_blocks, kv_heads, head_dim_v)) {
     return VPP_ERR_INVALID;
   }
 
@@ -485,7 +520,7 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
     p.kv_heads = kv_heads;
     p.group = heads / kv_heads;
     p.num_blocks = num_blocks;
-    p.paged = fp8 ? 0 : 1;
+    p.paged = widen ? 0 : 1;
     p.scale_log2 = scale_log2;
     p.block_table = block_table;
     p.out = static_cast<uint16_t*>(out);
@@ -509,7 +544,7 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
         s.n_splits = 1;
         s.split_keys = 0;
         s.cta_begin = (int32_t)cta;
-        s.kv_base = fp8 ? (int32_t)kv_base[i0 + i] : 0;
+        s.kv_base = widen ? (int32_t)kv_base[i0 + i] : 0;
         s.ws_row0 = 0;
         cta += (int64_t)s.n_pairs * kv_heads;
       }
@@ -517,7 +552,8 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
         err = VPP_ERR_INVALID;
         break;
       }
-      if (launch_chunk_attn(head_dim_qk, head_dim_v, tm_q, tm_k, tm_v, p, (int)cta, st) != cudaSuccess) {
+      if (launch_chunk_attn(head_dim_qk, head_dim_v, fp8 && !widen, tm_q, tm_k, tm_v, p, (int)cta, st) !=
+          cudaSuccess) {
         err = VPP_ERR_CUDA;
         break;
       }
@@ -791,53 +827,64 @@ int vpp_kv_append_varlen_fp8(const void* k_new, const void* v_new, void* k_cache
   return VPP_OK;
 }
 
+// Bytes of the bf16 copy of keys 0 .. prefix_len + chunk_len - 1.
+size_t fp8_widen_bytes(int64_t n, int kv_heads, int dq, int dv) {
+  return round_up((size_t)n * kv_heads * dq * 2, 256) + round_up((size_t)n * kv_heads * dv * 2, 256);
+}
+
 int vpp_chunk_attn_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                        const float* v_scale, const int32_t* block_table, int32_t num_blocks,
                        int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads, int head_dim_qk,
                        int head_dim_v, float softmax_scale, int num_splits, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream) {
   const int64_t P = prefix_len, C = chunk_len;
-  if (P < 0 || C < 0 || num_blocks <= 0 || num_splits < 0) return VPP_ERR_INVALID;
-  if (C == 0) return VPP_OK;
-  if (!q || !k_cache || !v_cache || !out || !scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
-  if (int r = check_heads(heads, kv_heads)) return r;
-  if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-    return VPP_ERR_INVALID;
-  if (P + C > (int64_t)INT32_MAX / 2) return VPP_ERR_INVALID;
-  if (block_table ? (int64_t)num_blocks * kBlockTokens < P + C : (int64_t)num_blocks < P + C)
-    return VPP_ERR_INVALID;
-  const int64_t n = P + C;
-  const size_t kb = round_up((size_t)n * kv_heads * head_dim_qk * 2, 256);
-  const size_t wb = kb + round_up((size_t)n * kv_heads * head_dim_v * 2, 256);
-  const size_t rest = vpp_chunk_attn_workspace_size(VPP_BF16, P, C, heads, kv_heads, head_dim_qk,
-                                                    head_dim_v, num_splits);
-  if (!workspace || workspace_bytes < wb + rest || !aligned16(workspace)) return VPP_ERR_WORKSPACE;
-  DeviceState* ds = nullptr;
-  if (int r = device_state(&ds)) return r;
+  if (C > 0 && !scales_ok(k_scale, v_scale)) return VPP_ERR_INVALID;
   cudaStream_t st = as_stream(stream);
-  static WidenPlan zero_plan;
-  WidenPlan wp = zero_plan;
-  wp.n = 1;
-  wp.base[1] = n;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws);
-  uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + kb);
-  if (launch_kv_widen_fp8(k_cache, v_cache, k16, v16, kv_heads, head_dim_qk, head_dim_v, block_table,
-                          num_blocks, wp, ds->status, ds->num_sms, st) != cudaSuccess)
-    return VPP_ERR_CUDA;
-  return chunk_attn_impl(q, VPP_BF16, k16, v16, nullptr, (int32_t)n, P, C, heads, kv_heads, head_dim_qk,
-                         head_dim_v, softmax_scale, num_splits, out, lse, ws + wb, workspace_bytes - wb,
-                         st, k_scale, v_scale);
+  if (P >= 0 && C > 0 && P + C <= (int64_t)INT32_MAX / 2 && kv_heads > 0 && head_dim_qk > 0 && head_dim_v > 0 &&
+      num_splits >= 0 && workspace && aligned16(workspace) && k_cache && v_cache && num_blocks > 0 &&
+      (block_table ? (int64_t)num_blocks * kBlockTokens >= P + C : (int64_t)num_blocks >= P + C) &&
+      check_heads(heads, kv_heads) == VPP_OK && supported_dims(head_dim_qk, head_dim_v)) {
+    const int64_t n = P + C;
+    const size_t wb = fp8_widen_bytes(n, kv_heads, head_dim_qk, head_dim_v);
+    const size_t rest = vpp_chunk_attn_workspace_size(VPP_BF16, P, C, heads, kv_heads, head_dim_qk,
+                                                      head_dim_v, num_splits);
+    if (workspace_bytes >= wb + rest) {
+      // The caller gave room for a bf16 copy of the visible keys: widen them
+      // once and run the bf16 kernel on it.
+      DeviceState* ds = nullptr;
+      if (int r = device_state(&ds)) return r;
+      static WidenPlan zero_plan;
+      WidenPlan wp = zero_plan;
+      wp.n = 1;
+      wp.base[1] = n;
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      uint16_t* k16 = reinterpret_cast<uint16_t*>(ws);
+      uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + round_up((size_t)n * kv_heads * head_dim_qk * 2, 256));
+      if (!aligned16(q) || !q || !out) return VPP_ERR_INVALID;
+      if (launch_kv_widen_fp8(k_cache, v_cache, k16, v16, kv_heads, head_dim_qk, head_dim_v, block_table,
+                              num_blocks, wp, ds->status, ds->num_sms, st) != cudaSuccess)
+        return VPP_ERR_CUDA;
+      return chunk_attn_impl(q, VPP_BF16, k16, v16, nullptr, (int32_t)n, P, C, heads, kv_heads, head_dim_qk,
+                             head_dim_v, softmax_scale, num_splits, out, lse, ws + wb, workspace_bytes - wb, st,
+                             k_scale, v_scale);
+    }
+  }
+  // The fp8 kernel reads the codes and widens them in shared memory.
+  return chunk_attn_impl(q, VPP_BF16, k_cache, v_cache, block_table, num_blocks, prefix_len, chunk_len, heads,
+                         kv_heads, head_dim_qk, head_dim_v, softmax_scale, num_splits, out, lse, workspace,
+                         workspace_bytes, st, k_scale, v_scale, true);
 }
 
 size_t vpp_chunk_attn_fp8_workspace_size(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
                                          int head_dim_qk, int head_dim_v, int num_splits) {
+  return vpp_chunk_attn_workspace_size(VPP_BF16, prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
+                                       head_dim_v, num_splits);
+}
+
+size_t vpp_chunk_attn_fp8_widen_workspace_size(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
+                                               int head_dim_qk, int head_dim_v, int num_splits) {
   if (prefix_len < 0 || chunk_len <= 0 || kv_heads <= 0 || head_dim_qk <= 0 || head_dim_v <= 0) return 0;
-  const int64_t n = prefix_len + chunk_len;
-  return round_up((size_t)n * kv_heads * head_dim_qk * 2, 256) +
-         round_up((size_t)n * kv_heads * head_dim_v * 2, 256) +
+  return fp8_widen_bytes(prefix_len + chunk_len, kv_heads, head_dim_qk, head_dim_v) +
          vpp_chunk_attn_workspace_size(VPP_BF16, prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
                                        head_dim_v, num_splits);
 }
@@ -857,6 +904,14 @@ int vpp_mixed_attn_fp8(const void* q, const void* k_cache, const void* v_cache, 
 size_t vpp_mixed_attn_fp8_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
                                          int32_t batch, int heads, int kv_heads, int head_dim_qk,
                                          int head_dim_v) {
+  if (!cu_seqlens_q || !ctx_lens || batch <= 0 || batch > kMaxBatch) return 0;
+  if (check_heads(heads, kv_heads) != VPP_OK) return 0;
+  return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v);
+}
+
+size_t vpp_mixed_attn_fp8_widen_workspace_size(const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                               int32_t batch, int heads, int kv_heads, int head_dim_qk,
+                                               int head_dim_v) {
   if (!cu_seqlens_q || !ctx_lens || batch <= 0 || batch > kMaxBatch) return 0;
   if (check_heads(heads, kv_heads) != VPP_OK) return 0;
   return decode_ws_bytes(cu_seqlens_q, ctx_lens, batch, heads, kv_heads, head_dim_qk, head_dim_v) +

@@ -54,19 +54,28 @@ constexpr int kAttnThreads = 384;  // warp 0 TMA, warps 1/3 MMA, warp 2 TMEM, WG
 constexpr int kSmemLimit = 232448; // 227 KB per CTA on sm_103a
 constexpr int kSubTileBytes = kTileN * 64 * 2;  // 128 keys x 64 bf16 (one 128B-swizzled block)
 
+// fp8 (E4M3) cache: the codes of one sub-tile (128 keys x 64 dims, one byte
+// each) land in a staging slot first and are widened into a ring slot.
+constexpr int kStageBytes = kTileN * 64;
+constexpr int kNumStages = 4;
+
 __host__ __device__ constexpr int attn_q_bytes(int dq) { return 2 * (dq / 64) * kSubTileBytes; }
+__host__ __device__ constexpr int attn_stage_bytes(bool f8) { return f8 ? kNumStages * kStageBytes : 0; }
 // The K/V ring is made of 16 KB sub-tile slots (128 keys x 64 dims); a K tile
 // takes dq/64 consecutive slots and a V tile dv/64 (modulo the ring size).
-__host__ __device__ constexpr int attn_num_slots(int dq) {
-  return (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes > 12
+__host__ __device__ constexpr int attn_num_slots(int dq, bool f8 = false) {
+  return (kSmemLimit - attn_q_bytes(dq) - attn_stage_bytes(f8) - 2048) / kSubTileBytes > 12
              ? 12
-             : (kSmemLimit - attn_q_bytes(dq) - 2048) / kSubTileBytes;
+             : (kSmemLimit - attn_q_bytes(dq) - attn_stage_bytes(f8) - 2048) / kSubTileBytes;
 }
-__host__ __device__ constexpr int attn_smem_bytes(int dq, int dv) {
-  return 1024 + attn_q_bytes(dq) + attn_num_slots(dq) * kSubTileBytes + 1024 + 0 * dv;
+__host__ __device__ constexpr int attn_smem_bytes(int dq, int dv, bool f8 = false) {
+  return 1024 + attn_q_bytes(dq) + attn_num_slots(dq, f8) * kSubTileBytes + attn_stage_bytes(f8) + 1024 +
+         0 * dv;
 }
 
-cudaError_t launch_chunk_attn(int dq, int dv, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+// f8: K/V maps address E4M3 codes (uint8, no swizzle, box 64 dims x 64 keys)
+// and the kernel computes in f16; otherwise bf16 maps and bf16 arithmetic.
+cudaError_t launch_chunk_attn(int dq, int dv, bool f8, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const AttnParams& p, int grid,
                               cudaStream_t stream);
 

@@ -94,16 +94,24 @@ struct Ring {
   }
 };
 
-template <int DQ, int DV>
+template <int DQ, int DV, bool F8>
 struct Shape {
   static constexpr int NQC = DQ / 64;  // 64-dim sub-tiles of a K tile (and of Q)
   static constexpr int NVC = DV / 64;  // 64-dim sub-tiles of a V tile
-  static constexpr int NSLOT = attn_num_slots(DQ);
+  static constexpr int NSLOT = attn_num_slots(DQ, F8);
   static constexpr int NB = NSLOT;     // tile barriers (>= tiles that fit the ring)
+  static constexpr int NSTG = F8 ? kNumStages : 0;  // staging slots of E4M3 codes
+  static constexpr int NCONV = 2;                     // fp8: converter warps (0 and 2)
+  static_assert(!F8 || (NSTG % NCONV == 0 && NB % 2 == 0),
+                "fp8: whole staging slots per converter; K tiles on even FULL barriers");
   static constexpr int QBYTES = attn_q_bytes(DQ);
-  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kTileN, false, false);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, DV, false, true);
-  static constexpr uint32_t IDESC_PV64 = idesc_bf16_f32(kTileM, 64, false, true);
+  // Operands are bf16, or f16 over an fp8 cache (E4M3 widens exactly to f16).
+  static constexpr uint32_t IDESC_QK =
+      F8 ? idesc_f16_f32(kTileM, kTileN, false, false) : idesc_bf16_f32(kTileM, kTileN, false, false);
+  static constexpr uint32_t IDESC_PV =
+      F8 ? idesc_f16_f32(kTileM, DV, false, true) : idesc_bf16_f32(kTileM, DV, false, true);
+  static constexpr uint32_t IDESC_PV64 =
+      F8 ? idesc_f16_f32(kTileM, 64, false, true) : idesc_bf16_f32(kTileM, 64, false, true);
   // P V of a tile runs as two MMA chains over 16-key steps: the first covers
   // keys [0, 16 * PV0) and starts once the softmax has stored their P, while
   // the softmax still computes the exponentials of the remaining keys.  With
@@ -113,9 +121,10 @@ struct Shape {
   static constexpr int KP0 = 16 * PV0;  // keys of the first part
   static constexpr bool SPLIT_P = PV0 < kTileN / 16;  // PV0 = 8: one chain
   static_assert(PV0 >= 1 && PV0 <= kTileN / 16, "P V chain split out of range");
-  // barrier indices: Q, S[2], P0[2], O[2], FINAL[2], TMP, P1[2], FULL[NB], EMPTY[NB]
+  // barrier indices: Q, S[2], P0[2], O[2], FINAL[2], TMP, P1[2], FULL[NB], EMPTY[NB],
+  // STAGE[NSTG]
   static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_P1 = 10,
-                       B_FULL = 12, B_EMPTY = 12 + NB, NBARS = 12 + 2 * NB;
+                       B_FULL = 12, B_EMPTY = 12 + NB, B_STG = 12 + 2 * NB, NBARS = 12 + 2 * NB + NSTG;
   static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
   // With d_qk = 192 the ring holds under two K/V tile pairs, and the next K
   // tile can only start once V_{j-1} is free: V_{j-1} is released by its own
@@ -142,7 +151,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* st
 // row, two lanes of work per packed instruction, stored to TMEM as bf16 pairs
 // (column c of the tile holds keys 2c, 2c + 1) every 16 keys, so that packed
 // values do not pile up in registers; the fp32 values are added to rs4.
-template <int K0, int K1>
+template <int K0, int K1, bool F16>
 __device__ __forceinline__ void exps_to_tmem(const float (&sv)[128], float2 sl2, float2 nmb2,
                                              float2 (&rs4)[4], uint32_t tS) {
   static_assert(K0 % 16 == 0 && K1 % 16 == 0, "parts are whole 16-key MMA steps");
@@ -156,7 +165,7 @@ __device__ __forceinline__ void exps_to_tmem(const float (&sv)[128], float2 sl2,
       const float a = ex2_approx(xx.x);
       const float b = ex2_approx(xx.y);
       rs4[c & 3] = fadd2(rs4[c & 3], make_float2(a, b));
-      pk[i] = pack_bf16x2(a, b);
+      pk[i] = F16 ? pack_half2(a, b) : pack_bf16x2(a, b);
     }
     tmem_st8(tS + 8 * k, pk);
   }
@@ -164,20 +173,21 @@ __device__ __forceinline__ void exps_to_tmem(const float (&sv)[128], float2 sl2,
 
 }  // namespace attn_detail
 
-template <int DQ, int DV>
+template <int DQ, int DV, bool F8>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     chunk_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ AttnParams p) {
   using namespace attn_detail;
-  using S = Shape<DQ, DV>;
+  using S = Shape<DQ, DV, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + S::QBYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + S::NSLOT * kSubTileBytes);
+  uint8_t* sStage = sRing + S::NSLOT * kSubTileBytes;  // fp8 cache only
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + S::NSTG * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
   volatile int* turn = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -220,9 +230,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(bar(S::B_TMP), 1);
     for (int i = 0; i < S::NB; ++i) {
-      mbar_init(bar(S::B_FULL + i), 1);
+      // over an fp8 cache a tile is full once each of its sub-tiles is widened
+      // (K tiles, even t, use even barriers)
+      mbar_init(bar(S::B_FULL + i), F8 ? ((i & 1) ? S::NVC : S::NQC) : 1);
       mbar_init(bar(S::B_EMPTY + i), 2);  // released by both MMA issuers
     }
+    for (int i = 0; i < S::NSTG; ++i) mbar_init(bar(S::B_STG + i), 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -240,7 +253,158 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // setmaxnreg so that the code it dominates is compiled for that budget.
   if (warp < 4) {
     regs_dec<kRegsLow>();
-    if (warp == 0 && lane == 0) {
+    if constexpr (F8) {
+      // ------------------------------------- producer over an fp8 cache
+      // The K/V codes of a sub-tile (128 keys x 64 dims) are copied by TMA
+      // into a staging slot, then warp 0 widens them exactly to f16 (each
+      // value times 2^-8, which the score scale and the final division undo)
+      // in the 128B-swizzled ring slot layout the MMAs read (the layout TMA
+      // writes for a bf16 cache), zeroing rows past the sequence (the pool
+      // holds whatever codes there), and signals the tile's FULL barrier.  Q is
+      // loaded as bf16 and turned into f16 in place by the 128 threads of
+      // this warpgroup before any MMA; the first staging copies are in flight
+      // meanwhile.
+      auto block_coord = [&](int b) -> int {
+        if (b * kBlockTokens >= seg.kv_len) return p.num_blocks;  // reads zeros
+        const int e = p.block_table[seg.table_off + b];
+        if (e < 0 || e >= p.num_blocks) {
+          record_status(p.status, kStatusInvalid);
+          return p.num_blocks;
+        }
+        return e;
+      };
+      constexpr int kPerPair = S::NQC + S::NVC;  // sub-tiles per K/V tile pair
+      constexpr int kSlotsPerWarp = S::NSTG / S::NCONV;
+      const int total = n_kv * kPerPair;
+      const int cw = warp >> 1;  // converter index of warps 0 and 2
+      // Sub-tile u (order K_0's, V_0's, K_1's, ...) is widened by converter
+      // u % NCONV through that warp's staging slots, in turn.
+      auto stage_slot = [&](int u) { return cw * kSlotsPerWarp + (u / S::NCONV) % kSlotsPerWarp; };
+      auto stage_parity = [&](int u) { return static_cast<uint32_t>((u / S::NCONV) / kSlotsPerWarp) & 1u; };
+      // Starts the copy of sub-tile u's codes into its staging slot (one lane).
+      auto issue_stage = [&](int u) {
+        const int j = u / kPerPair;
+        const int r = u - j * kPerPair;
+        const bool is_v = r >= S::NQC;
+        const int c = is_v ? r - S::NQC : r;
+        const int key0 = k_lo + j * kTileN;
+        int c0, c1;
+        if (p.paged) {
+          c0 = block_coord(key0 / kBlockTokens);
+          c1 = block_coord(key0 / kBlockTokens + 1);
+        } else {
+          c0 = seg.kv_base + key0;
+          c1 = c0 + kBlockTokens;
+        }
+        const int slot = stage_slot(u);
+        const uint32_t sb = bar(S::B_STG + slot);
+        const uint32_t d = smem_u32(sStage + slot * kStageBytes);
+        const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(sb, kStageBytes);
+        if (p.paged) {
+          tma_load_4d(d, m, sb, c * 64, g, 0, c0);
+          tma_load_4d(d + kStageBytes / 2, m, sb, c * 64, g, 0, c1);
+        } else {
+          tma_load_3d(d, m, sb, c * 64, g, c0);
+          tma_load_3d(d + kStageBytes / 2, m, sb, c * 64, g, c1);
+        }
+      };
+      const bool converter = (warp & 1) == 0 && cw < S::NCONV;
+      int issued = cw;  // next sub-tile whose staging copy this warp starts (lane 0)
+      if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(bar(S::B_Q), 2 * S::NQC * kSubTileBytes);
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < S::NQC; ++c)
+            tma_load_4d(smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes), &tm_q, bar(S::B_Q),
+                        c * 64, 0, g, seg.q_start + tok0 + x * T);
+      }
+      if (converter && lane == 0)
+        for (int n = 0; n < kSlotsPerWarp && issued < total; ++n, issued += S::NCONV) issue_stage(issued);
+      const bool qok = warp_wait(bar(S::B_Q), 0, p.status, abort_flag);
+      if (qok) {
+        // bf16 -> f16, 16 bytes per step; an element outside f16's range
+        // (|q| > 65504) becomes infinite and is reported as invalid input.
+        uint32_t amax = 0u;
+        for (int ch = threadIdx.x; ch < 2 * S::NQC * (kSubTileBytes / 16); ch += 128) {
+          uint4* qp = reinterpret_cast<uint4*>(sQ + ch * 16);
+          uint4 w = *qp;
+          uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            wv[i] = pack_half2(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xFFFF0000u));
+            amax = __vmaxu2(amax, wv[i] & 0x7FFF7FFFu);
+          }
+          *qp = w;
+        }
+        if ((amax & 0xFFFFu) >= 0x7C00u || (amax >> 16) >= 0x7C00u) record_status(p.status, kStatusInvalid);
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four warps of this warpgroup
+      if (converter) {
+        bool ok = qok;
+        int rq = 0;     // next tile whose release has not been observed
+        int done = cw;  // next sub-tile of this warp whose staging slot is not consumed
+        for (int u = cw; ok && u < total; u += S::NCONV) {
+          const int j = u / kPerPair;
+          const int r = u - j * kPerPair;
+          const int part = r >= S::NQC ? 1 : 0;
+          const int c = part ? r - S::NQC : r;
+          const int t = 2 * j + part;
+          const int pos = S::tile_pos(t);
+          const int nsub = S::tile_slots(t);
+          // Tiles are released in load order: wait until every tile that used
+          // these slots, and the tile that last used this barrier, is
+          // released.
+          while (rq < t && (rq <= t - S::NB || S::tile_pos(rq) < pos + nsub - S::NSLOT)) {
+            if (!(ok = warp_wait(bar(S::B_EMPTY + rq % S::NB), (rq / S::NB) & 1u, p.status, abort_flag)))
+              break;
+            ++rq;
+          }
+          if (!ok) break;
+          const int slot = stage_slot(u);
+          if (!(ok = warp_wait(bar(S::B_STG + slot), stage_parity(u), p.status, abort_flag))) break;
+          const uint8_t* src = sStage + slot * kStageBytes;
+          uint8_t* dst = sRing + ((pos + c) % S::NSLOT) * kSubTileBytes;
+          const int valid_rows = seg.kv_len - (k_lo + j * kTileN);
+#pragma unroll 4
+          for (int it = 0; it < kTileN * 4 / 32; ++it) {
+            const int idx = it * 32 + lane;
+            const int row = idx >> 2;  // key within the tile
+            const int q4 = idx & 3;    // 16 codes: dims 16 q4 .. 16 q4 + 15
+            uint4 w = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
+            if (row >= valid_rows) w = make_uint4(0u, 0u, 0u, 0u);
+            uint32_t h[8];
+            widen_e4m3x4_scaled(w.x, h[0], h[1]);
+            widen_e4m3x4_scaled(w.y, h[2], h[3]);
+            widen_e4m3x4_scaled(w.z, h[4], h[5]);
+            widen_e4m3x4_scaled(w.w, h[6], h[7]);
+            uint8_t* rp = dst + row * 128;
+            *reinterpret_cast<uint4*>(rp + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(rp + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          done = u + S::NCONV;
+          if (lane == 0) {
+            mbar_arrive(bar(S::B_FULL + t % S::NB));  // one of the tile's nsub arrivals
+            if (issued < total) {
+              issue_stage(issued);
+              issued += S::NCONV;
+            }
+          }
+        }
+        if (!ok && lane == 0) {
+          // Let every copy this warp started land before the CTA exits.
+          for (int v = done; v < issued; v += S::NCONV)
+            mbar_wait_for(bar(S::B_STG + stage_slot(v)), stage_parity(v), kCleanupNs);
+        }
+        if (!qok && warp == 0 && lane == 0) mbar_wait_for(bar(S::B_Q), 0, kCleanupNs);
+      }
+    }
+    if (!F8 && warp == 0 && lane == 0) {
       // ---------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -351,7 +515,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr uint32_t kSub16 = kSubTileBytes >> 4;
       const uint32_t tS = tbase + x * kTileN;
       const uint32_t tO = tbase + 2 * kTileN + x * DV;
-      bool ok = mbar_wait(bar(S::B_Q), 0, p.status, abort_flag);
+      // (over an fp8 cache Q was widened by this warpgroup before this point)
+      bool ok = F8 ? *abort_flag == 0u : mbar_wait(bar(S::B_Q), 0, p.status, abort_flag);
       // Ring slots of K_j and V_{j-1}, advanced by one tile pair per block.
       int kslot = 0;
       int vslot = S::NQC - (S::NQC + S::NVC);  // becomes V_0's slot at j = 1
@@ -474,8 +639,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tO = lane_base + 2 * kTileN + x * DV;
     // Per-kv-head factors of an fp8 cache (key codes x k_scale, values x
     // v_scale): k_scale joins the score scale, v_scale the final division.
-    const float sl = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
-    const float vsc = p.v_scale ? __ldg(p.v_scale + g) : 1.f;
+    // Over an fp8 cache the widened operands are the values times 2^-8.
+    constexpr float kWidenUndo = F8 ? 256.f : 1.f;
+    const float sl = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + g) * kWidenUndo : p.scale_log2;
+    const float vsc = p.v_scale ? __ldg(p.v_scale + g) * kWidenUndo : 1.f;
     float m = -INFINITY;  // running max of score * scale * log2(e)
     float l = 0.f;        // running denominator, relative to 2^m
     bool ok = true;
@@ -522,7 +689,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto part = [&](auto k0, auto k1, float mref) {
         const float mb = (mref == -INFINITY) ? 0.f : mref;
         const float2 nmb2 = make_float2(-mb, -mb);
-        exps_to_tmem<decltype(k0)::value, decltype(k1)::value>(sv, sl2, nmb2, rs4, tS);
+        exps_to_tmem<decltype(k0)::value, decltype(k1)::value, F8>(sv, sl2, nmb2, rs4, tS);
       };
       using K_0 = std::integral_constant<int, 0>;
       using K_P0 = std::integral_constant<int, S::KP0>;
@@ -634,23 +801,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-template <int DQ, int DV>
+template <int DQ, int DV, bool F8>
 cudaError_t launch_chunk_attn_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const AttnParams& p, int grid,
                                 cudaStream_t stream) {
-  constexpr int smem = attn_smem_bytes(DQ, DV);
+  constexpr int smem = attn_smem_bytes(DQ, DV, F8);
   static_assert(smem <= kSmemLimit, "shared memory budget");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(chunk_attn_kernel<DQ, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chunk_attn_kernel<DQ, DV, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  chunk_attn_kernel<DQ, DV><<<grid, kAttnThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+  chunk_attn_kernel<DQ, DV, F8><<<grid, kAttnThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 

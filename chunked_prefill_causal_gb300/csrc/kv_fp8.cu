@@ -1,5 +1,5 @@
 // kv_fp8.cu -- fp8 (E4M3) KV cache: quantising append, and the exact widening
-// of cached codes to bf16 that the chunk-attention kernel reads.
+// of cached codes to bf16 for callers that trade workspace for prefill speed.
 //
 // "02 · 并行策略与 PP 切分" (deployment note), §1 and §3.2: the KV cache is
 // kept in fp8, about half the bytes per token of bf16, which nearly doubles
@@ -13,10 +13,12 @@
 // bf16 values (32 bytes) into 16 codes (one 16-byte store); HBM-bound:
 // 3 bytes per element (2 read, 1 written).
 //
-// Widening: every E4M3 value is exactly a bf16 value, so the codes are
-// widened to bf16 without their scales (3 bytes per element again) and the
-// scales are applied by the attention kernel (k_scale in the score scale,
-// v_scale on the output), leaving the arithmetic exact.
+// Widening (optional prefill path): every E4M3 value is exactly a bf16
+// value, so a caller that provides a workspace for the bf16 copy of the
+// visible keys gets them widened once, without their scales (3 bytes per
+// element again), and the bf16 attention kernel applies the scales (k_scale
+// in the score scale, v_scale on the output), leaving the arithmetic exact.
+// Without that workspace the fp8 attention kernel widens the codes itself.
 #include "common.cuh"
 #include "fp8.cuh"
 #include "ptx.cuh"
@@ -52,6 +54,17 @@ __device__ __forceinline__ uint4 quantise16(const uint4 a, const uint4 b, float 
     out[i] = lo | (hi << 16);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Two E4M3 codes to two floats (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  float2 f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(h2));
+  return f;
 }
 
 // 16 E4M3 codes -> 16 bf16 values (exact).

@@ -13,22 +13,28 @@
 
 namespace vpp {
 
-template <int DQ, int DV>
+template <int DQ, int DV, bool F8>
 cudaError_t launch_chunk_attn_t(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                 const AttnParams&, int, cudaStream_t);
 
-cudaError_t launch_chunk_attn(int dq, int dv, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+template <bool F8>
+cudaError_t launch_chunk_attn_f(int dq, int dv, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                                cudaStream_t stream) {
+  if (dq == 64 && dv == 64) return launch_chunk_attn_t<64, 64, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (dq == 64 && dv == 128) return launch_chunk_attn_t<64, 128, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (dq == 128 && dv == 64) return launch_chunk_attn_t<128, 64, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (dq == 128 && dv == 128) return launch_chunk_attn_t<128, 128, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (dq == 192 && dv == 64) return launch_chunk_attn_t<192, 64, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (dq == 192 && dv == 128) return launch_chunk_attn_t<192, 128, F8>(tm_q, tm_k, tm_v, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_chunk_attn(int dq, int dv, bool f8, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const AttnParams& p, int grid,
                               cudaStream_t stream) {
-  if (dq == 64 && dv == 64) return launch_chunk_attn_t<64, 64>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (dq == 64 && dv == 128) return launch_chunk_attn_t<64, 128>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (dq == 128 && dv == 64) return launch_chunk_attn_t<128, 64>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (dq == 128 && dv == 128)
-    return launch_chunk_attn_t<128, 128>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (dq == 192 && dv == 64) return launch_chunk_attn_t<192, 64>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (dq == 192 && dv == 128)
-    return launch_chunk_attn_t<192, 128>(tm_q, tm_k, tm_v, p, grid, stream);
-  return cudaErrorInvalidValue;
+  return f8 ? launch_chunk_attn_f<true>(dq, dv, tm_q, tm_k, tm_v, p, grid, stream)
+            : launch_chunk_attn_f<false>(dq, dv, tm_q, tm_k, tm_v, p, grid, stream);
 }
 
 namespace {

@@ -261,6 +261,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with f16 A and B (format 0) and f32
+// accumulation; otherwise as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------ register budgets
 // Moves registers between warpgroups: every warp of a warpgroup executes the
 // same call.  The block's total (threads x registers at launch) bounds the sum.
@@ -316,7 +323,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Packs two floats to f16x2 with round-to-nearest-even: `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ------------------------------------------------------------------ fp8 E4M3
+// Four E4M3 codes (byte i of w = code i) -> two f16x2 words (lo: codes 0, 1;
+// hi: codes 2, 3) holding each code's value times 2^-8, exactly.
+//
+// E4M3 (bias 7) and f16 (bias 15) put exponent and mantissa in the same
+// order, so the code's seven magnitude bits placed at f16 bits 7..13 give an
+// f16 whose exponent field is the code's and whose value is the code's value
+// scaled by 2^(7-15), for normal and subnormal codes alike (0 stays 0); the
+// sign moves from bit 7 to bit 15.  Integer operations only: each byte is
+// spread to its own 16-bit lane, x + (x & 0x80) moves the sign bit to bit 8
+// (no carry leaves the lane), and << 7 aligns both.  The NaN codes 0x7F and
+// 0xFF come out as +-480 instead (the append never writes them).
+__device__ __forceinline__ void widen_e4m3x4_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t x0, x1;
+  asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(x0) : "r"(w));
+  asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(x1) : "r"(w));
+  lo = (x0 + (x0 & 0x00800080u)) << 7;
+  hi = (x1 + (x1 & 0x00800080u)) << 7;
+}
+
 // Two E4M3 codes (lo = the byte at the lower address) from two floats, round
 // to nearest even, magnitudes beyond the largest finite value (448) clamped.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
@@ -325,15 +358,5 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Two E4M3 codes to two floats (exact: every E4M3 value is an f16 value).
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-  float2 f;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-      : "=f"(f.x), "=f"(f.y)
-      : "r"(h2));
-  return f;
-}
 
 }  // namespace vpp

@@ -51,10 +51,12 @@ SIGNATURES = {
                             _int, _int, _int, _int, _f32, _int, _c_void_p, _c_void_p, _c_void_p, _sz,
                             _c_void_p], _int),
     "vpp_chunk_attn_fp8_workspace_size": ([_i64, _i64, _int, _int, _int, _int, _int], _sz),
+    "vpp_chunk_attn_fp8_widen_workspace_size": ([_i64, _i64, _int, _int, _int, _int, _int], _sz),
     "vpp_mixed_attn_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
                             _c_void_p, _c_void_p, _i32, _int, _int, _int, _int, _f32, _c_void_p, _c_void_p,
                             _c_void_p, _sz, _c_void_p], _int),
     "vpp_mixed_attn_fp8_workspace_size": ([_c_void_p, _c_void_p, _i32, _int, _int, _int, _int], _sz),
+    "vpp_mixed_attn_fp8_widen_workspace_size": ([_c_void_p, _c_void_p, _i32, _int, _int, _int, _int], _sz),
     "vpp_topk_chunk_attn": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64, _i64, _c_void_p, _c_void_p,
                              _i32, _int, _int, _int, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p], _int),
     "vpp_topk_chunk_attn_fp8": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i64,
@@ -310,9 +312,17 @@ def chunk_attn_fp8_workspace_size(prefix_len, chunk_len, heads, kv_heads, dq, dv
                                                         dq, dv, num_splits))
 
 
+def chunk_attn_fp8_widen_workspace_size(prefix_len, chunk_len, heads, kv_heads, dq, dv, num_splits=0):
+    return int(load().vpp_chunk_attn_fp8_widen_workspace_size(int(prefix_len), int(chunk_len), heads, kv_heads,
+                                                              dq, dv, num_splits))
+
+
 def vpp_chunk_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, prefix_len, block_table=None, out=None,
-                       lse=None, softmax_scale=0.0, num_splits=0, workspace=None, stream=None):
-    """Chunk attention over an E4M3 cache (bf16 q), paged or contiguous."""
+                       lse=None, softmax_scale=0.0, num_splits=0, workspace=None, stream=None, widen=False):
+    """Chunk attention over an E4M3 cache (bf16 q), paged or contiguous.  The
+    kernel widens the codes itself unless the workspace also holds a bf16
+    copy of the visible keys (widen=True allocates one when no workspace is
+    given)."""
     _need_cuda(q, k_cache, v_cache, block_table, out, lse, workspace)
     _fp8_cache(k_cache, v_cache)
     C, H, dq = q.shape
@@ -322,7 +332,8 @@ def vpp_chunk_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, prefix_len, block_
     if out is None:
         out = torch.empty((C, H, dv), dtype=torch.bfloat16, device=q.device)
     if workspace is None:
-        need = chunk_attn_fp8_workspace_size(prefix_len, C, H, Hkv, dq, dv, num_splits)
+        size = chunk_attn_fp8_widen_workspace_size if widen else chunk_attn_fp8_workspace_size
+        need = size(prefix_len, C, H, Hkv, dq, dv, num_splits)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     wbytes = workspace.numel() * workspace.element_size()
     _check("vpp_chunk_attn_fp8", load().vpp_chunk_attn_fp8(
@@ -338,9 +349,16 @@ def mixed_attn_fp8_workspace_size(cu_seqlens_q, ctx_lens, heads, kv_heads, dq, d
     return int(load().vpp_mixed_attn_fp8_workspace_size(cu_p, ctx_p, len(ctx), heads, kv_heads, dq, dv))
 
 
+def mixed_attn_fp8_widen_workspace_size(cu_seqlens_q, ctx_lens, heads, kv_heads, dq, dv):
+    cu, cu_p = _i32_host(cu_seqlens_q)
+    ctx, ctx_p = _i32_host(ctx_lens)
+    return int(load().vpp_mixed_attn_fp8_widen_workspace_size(cu_p, ctx_p, len(ctx), heads, kv_heads, dq, dv))
+
+
 def vpp_mixed_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, ctx_lens, out=None,
-                       lse=None, softmax_scale=0.0, workspace=None, stream=None):
-    """Mixed micro-batch over an E4M3 paged cache (host cu_seqlens_q / ctx_lens)."""
+                       lse=None, softmax_scale=0.0, workspace=None, stream=None, widen=False):
+    """Mixed micro-batch over an E4M3 paged cache (host cu_seqlens_q / ctx_lens);
+    widen as for vpp_chunk_attn_fp8."""
     _need_cuda(q, k_cache, v_cache, block_table, out, lse, workspace)
     _fp8_cache(k_cache, v_cache)
     T, H, dq = q.shape
@@ -351,7 +369,7 @@ def vpp_mixed_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, cu_se
     ctx, ctx_p = _i32_host(ctx_lens)
     if out is None:
         out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
-    need = mixed_attn_fp8_workspace_size(cu, ctx, H, Hkv, dq, dv)
+    need = (mixed_attn_fp8_widen_workspace_size if widen else mixed_attn_fp8_workspace_size)(cu, ctx, H, Hkv, dq, dv)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -277,11 +277,21 @@ int vpp_kv_append_varlen_fp8(const void *k_new, const void *v_new,
 
 /*
  * a2..a7 over an fp8 cache: the contract of vpp_chunk_attn_ex with a bf16 q
- * and K, V read as code x scale.  The keys 0 .. prefix_len + chunk_len - 1
- * are first widened to bf16 in the workspace (exact: every E4M3 value is a
- * bf16 value); the attention kernel then multiplies scores by k_scale and the
- * output by v_scale of the row's kv head.  workspace: DEVICE, at least
- * vpp_chunk_attn_fp8_workspace_size(...) bytes, never NULL for chunk_len > 0.
+ * and K, V read as code x scale.  Two ways, chosen by the workspace size:
+ *  - workspace >= vpp_chunk_attn_fp8_workspace_size(...) (the key-split
+ *    partials only, as for vpp_chunk_attn_ex: 0 without a split, independent
+ *    of prefix_len): the kernel reads the codes and widens them to f16
+ *    operands in shared memory (exact: every E4M3 value is an f16 value),
+ *    turns q into f16 operands and applies k_scale to the scores and v_scale
+ *    to the output of the row's kv head.  No copy of the cache is made; every
+ *    CTA widens the tiles it reads, which costs prefill time.  q elements
+ *    must lie within f16's range (|q| <= 65504): a larger one is reported as
+ *    VPP_ERR_INVALID by vpp_last_device_status and its rows are not valid.
+ *  - workspace >= vpp_chunk_attn_fp8_widen_workspace_size(...): keys
+ *    0 .. prefix_len + chunk_len - 1 are first widened to bf16 in the
+ *    workspace (exact), once, and the bf16 kernel reads that copy (faster;
+ *    the copy grows with prefix_len).
+ * workspace: DEVICE, 16-byte aligned.
  */
 int vpp_chunk_attn_fp8(const void *q, const void *k_cache,
                        const void *v_cache, const float *k_scale,
@@ -292,18 +302,28 @@ int vpp_chunk_attn_fp8(const void *q, const void *k_cache,
                        int num_splits, void *out, float *lse, void *workspace,
                        size_t workspace_bytes, void *stream);
 
-/* Workspace bytes vpp_chunk_attn_fp8 needs for these arguments. */
+/* Workspace bytes vpp_chunk_attn_fp8 needs for these arguments (the
+ * in-kernel widening). */
 size_t vpp_chunk_attn_fp8_workspace_size(int64_t prefix_len,
                                          int64_t chunk_len, int heads,
                                          int kv_heads, int head_dim_qk,
                                          int head_dim_v, int num_splits);
 
+/* Workspace bytes with which vpp_chunk_attn_fp8 widens the visible keys to a
+ * bf16 copy first (the partials plus the copy). */
+size_t vpp_chunk_attn_fp8_widen_workspace_size(int64_t prefix_len,
+                                               int64_t chunk_len, int heads,
+                                               int kv_heads, int head_dim_qk,
+                                               int head_dim_v, int num_splits);
+
 /*
  * a8..a9 over an fp8 paged cache: the contract of vpp_mixed_attn.  Decode
- * rows read the codes directly (the decode kernel's shapes as in
- * vpp_mixed_attn); every other sequence with queries reads the bf16 widening
- * of its whole context from the workspace.  workspace >=
- * vpp_mixed_attn_fp8_workspace_size(...) bytes.
+ * rows (the decode kernel's shapes as in vpp_mixed_attn) read the codes
+ * directly.  The other sequences with queries go through the chunk-attention
+ * kernel as in vpp_chunk_attn_fp8: reading the codes (q within f16's range)
+ * with a workspace of vpp_mixed_attn_fp8_workspace_size(...) bytes (decode
+ * partials only), or a bf16 copy of their contexts widened into a workspace
+ * of vpp_mixed_attn_fp8_widen_workspace_size(...) bytes.
  */
 int vpp_mixed_attn_fp8(const void *q, const void *k_cache,
                        const void *v_cache, const float *k_scale,
@@ -321,6 +341,14 @@ size_t vpp_mixed_attn_fp8_workspace_size(const int32_t *cu_seqlens_q,
                                          int32_t batch, int heads,
                                          int kv_heads, int head_dim_qk,
                                          int head_dim_v);
+
+/* Workspace bytes with which vpp_mixed_attn_fp8 widens the chunk-attention
+ * sequences' contexts to bf16 first. */
+size_t vpp_mixed_attn_fp8_widen_workspace_size(const int32_t *cu_seqlens_q,
+                                               const int32_t *ctx_lens,
+                                               int32_t batch, int heads,
+                                               int kv_heads, int head_dim_qk,
+                                               int head_dim_v);
 
 /*
  * Top-k sparse prefix attention (DSA-style): [VPP review] §7 (sparse attention

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from chunked_prefill_causal_gb300 import vpp
@@ -88,9 +89,11 @@ def test_host_validation_rejects_bad_arguments(lib):
                                  null) == vpp.VPP_ERR_UNSUPPORTED
     assert lib.vpp_chunk_attn_fp8(fake, fake, fake, null, fake, fake, 2, 0, 29, 8, 2, 128, 128, 0.0, 0,
                                   fake, null, fake, 1 << 30, null) == vpp.VPP_ERR_INVALID
-    # fp8 chunk attention: the widening needs a workspace
-    assert lib.vpp_chunk_attn_fp8(fake, fake, fake, fake, fake, fake, 2, 0, 29, 8, 2, 128, 128, 0.0, 0,
-                                  fake, null, null, 0, null) == vpp.VPP_ERR_WORKSPACE
+    # fp8 chunk attention: an empty chunk is a no-op; unsupported dims are refused on the host
+    assert lib.vpp_chunk_attn_fp8(null, null, null, null, null, null, 2, 0, 0, 8, 2, 128, 128, 0.0, 0,
+                                  null, null, null, 0, null) == vpp.VPP_OK
+    assert lib.vpp_chunk_attn_fp8(fake, fake, fake, fake, fake, fake, 2, 0, 29, 8, 2, 96, 96, 0.0, 0,
+                                  fake, null, null, 0, null) == vpp.VPP_ERR_UNSUPPORTED
     assert lib.vpp_mixed_attn_fp8(fake, fake, fake, fake, null, fake, 4, 16, cu, ctx, 2, 8, 2, 128, 128,
                                   0.0, fake, null, null, 0, null) == vpp.VPP_ERR_INVALID
 
@@ -112,20 +115,6 @@ def test_topk_validation_and_workspace(lib):
     assert vpp.topk_chunk_attn_workspace_size(16, 2048, 8, 128) == 16 * 2 * 8 * 128 * 4 + 16 * 2 * 8 * 4
     assert lib.vpp_topk_chunk_attn_fp8(fake, fake, fake, null, fake, fake, 64, 0, 16, fake, fake, 1024, 8, 2, 128,
                                        0.0, fake, null, null, 0, null) == vpp.VPP_ERR_INVALID
-
-
-def test_fp8_workspace_sizes_are_host_side(lib):
-    # widened K and V of the visible keys (bf16), plus the split partials
-    P, C, H, Hkv, d = 1000, 200, 8, 2, 128
-    n = P + C
-    base = 2 * ((n * Hkv * d * 2 + 255) // 256 * 256)
-    assert vpp.chunk_attn_fp8_workspace_size(P, C, H, Hkv, d, d, 1) == base
-    assert vpp.chunk_attn_fp8_workspace_size(P, C, H, Hkv, d, d, 4) == \
-        base + vpp.chunk_attn_workspace_size(vpp.VPP_BF16, P, C, H, Hkv, d, d, 4)
-    # mixed: decode rows need no widening; the prefill sequence's whole context does
-    cu, ctx = [0, 1, 101], [5000, 400]
-    ws = vpp.mixed_attn_fp8_workspace_size(cu, ctx, H, Hkv, d, d)
-    assert ws == vpp.mixed_attn_workspace_size(cu, ctx, H, Hkv, d, d) + 2 * ((400 * Hkv * d * 2 + 255) // 256 * 256)
 
 
 def test_split_plan_is_host_side(lib):
@@ -159,3 +148,24 @@ def test_noalloc_host_checks_run_before_any_device_call(lib):
         vpp.VPP_ERR_INVALID
     assert f(fake, fake, fake, null, 256, 100, 16, 8, 2, 128, 128, ctypes.c_float(0.0), -1, fake, null, null) == \
         vpp.VPP_ERR_INVALID
+
+
+def test_fp8_workspace_does_not_grow_with_the_prefix(lib):
+    # The fp8 kernels widen the codes themselves: the workspace holds only
+    # key-split partials, whose size depends on the chunk, not on the prefix.
+    from chunked_prefill_causal_gb300 import vpp as v
+    C, H, Hkv, d = 4096, 32, 8, 128
+    assert v.chunk_attn_fp8_workspace_size(100000, C, H, Hkv, d, d, 1) == 0
+    a = v.chunk_attn_fp8_workspace_size(8192, C, H, Hkv, d, d, 2)
+    b = v.chunk_attn_fp8_workspace_size(500000, C, H, Hkv, d, d, 2)
+    assert a == b == v.chunk_attn_workspace_size(v.VPP_BF16, 8192, C, H, Hkv, d, d, 2) > 0
+    cu = np.array([0, 2048, 2049], dtype=np.int32)
+    for ctx in ([2048 + 16384, 900], [2048 + 122880, 900]):
+        assert v.mixed_attn_fp8_workspace_size(cu, np.array(ctx, dtype=np.int32), H, Hkv, d, d) == \
+            v.mixed_attn_workspace_size(cu, np.array(ctx, dtype=np.int32), H, Hkv, d, d) == 0
+        # the optional bf16 copy of the prefill sequence's context does grow with it
+        assert v.mixed_attn_fp8_widen_workspace_size(cu, np.array(ctx, dtype=np.int32), H, Hkv, d, d) == \
+            2 * ((ctx[0] * Hkv * d * 2 + 255) // 256 * 256)
+    n = 8192 + C
+    assert v.chunk_attn_fp8_widen_workspace_size(8192, C, H, Hkv, d, d, 2) == \
+        2 * ((n * Hkv * d * 2 + 255) // 256 * 256) + a

@@ -5,8 +5,9 @@ oracle's quantiser (oracle/fp8.py: the float32 quotient x / scale rounded to
 E4M3, ties to even, saturating at 448), including exact ties, quotients that
 tie only after float32 rounding, subnormal codes and saturation.  Attention
 over the fp8 cache is compared with the fp64 oracle run on the dequantised
-cache (code value x scale), to the bf16 path's tolerances: the widening to
-bf16 is exact and the scales are folded in float32.
+cache (code value x scale), to the bf16 path's tolerances: the kernels widen
+the codes exactly to f16 operands (every E4M3 value is an f16 value) and
+fold the scales in float32.
 """
 
 import math
@@ -181,7 +182,7 @@ def test_append_contiguous_and_varlen_place_the_same_codes():
 
 
 # ----------------------------------------------------------------- attention
-def run_fp8(P, C, Hq, Hkv, dq, dv, seed, num_splits=0, paged=True, append_chunk=None):
+def run_fp8(P, C, Hq, Hkv, dq, dv, seed, num_splits=0, paged=True, append_chunk=None, widen=False):
     std = 1 / math.sqrt(dq)
     q = gen((C, Hq, dq), seed, std)
     k = gen((P + C, Hkv, dq), seed + 1, std)
@@ -191,7 +192,7 @@ def run_fp8(P, C, Hq, Hkv, dq, dv, seed, num_splits=0, paged=True, append_chunk=
     cache = Fp8Cache(k, v, ks, vs, seed=seed, append_chunk=append_chunk, paged=paged)
     lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
     out = vpp.vpp_chunk_attn_fp8(q.to(DEV), cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table,
-                                 lse=lse, num_splits=num_splits)
+                                 lse=lse, num_splits=num_splits, widen=widen)
     torch.cuda.synchronize()
     assert vpp.vpp_last_device_status() == 0
     kq = ofp8.dequantize_kv(ofp8.quantize_kv(k.float().numpy(), ks), ks)
@@ -211,6 +212,9 @@ FP8_CASES = [  # P, C, Hq, Hkv, dq, dv, paged
     (700, 129, 4, 4, 192, 128, True),    # MLA-shaped
     (250, 90, 4, 2, 64, 64, True),
     (250, 90, 4, 2, 192, 64, False),
+    (333, 64, 8, 4, 64, 128, True),
+    (200, 200, 2, 1, 128, 64, False),
+    (1500, 260, 16, 2, 192, 128, True),  # MLA head dims, G = 8, many tiles
 ]
 
 
@@ -226,25 +230,81 @@ def test_fp8_split_prefix_matches(splits):
     run_fp8(2000, 100, 8, 2, 128, 128, seed=41, num_splits=splits)
 
 
-def test_fp8_workspace_is_required():
-    P, C, Hq, Hkv, d = 100, 28, 4, 1, 128
-    need = vpp.chunk_attn_fp8_workspace_size(P, C, Hq, Hkv, d, d)
-    assert need >= 2 * (P + C) * Hkv * d * 2
+@pytest.mark.parametrize("case", [(640, 37, 8, 2, 128, 128, True, 0), (700, 129, 4, 4, 192, 128, True, 3),
+                                  (250, 90, 4, 2, 192, 64, False, 0)],
+                         ids=["d128_paged", "d192_paged_split3", "d192-64_contig"])
+def test_fp8_widened_copy_path(case):
+    # with room for a bf16 copy of the visible keys the codes are widened once
+    # in HBM and the bf16 kernel reads the copy
+    P, C, Hq, Hkv, dq, dv, paged, splits = case
+    assert vpp.chunk_attn_fp8_widen_workspace_size(P, C, Hq, Hkv, dq, dv, splits) >= \
+        2 * (P + C) * Hkv * min(dq, dv) * 2
+    run_fp8(P, C, Hq, Hkv, dq, dv, seed=P + dq, paged=paged, num_splits=splits, widen=True)
+
+
+def test_fp8_workspace_holds_split_partials_only():
+    # The codes are widened inside the kernel: without a key split no
+    # workspace is needed, and a split needs its float32 partials (which do
+    # not depend on the prefix length), refused when the buffer is short.
+    P, C, Hq, Hkv, d = 3000, 28, 4, 1, 128
+    assert vpp.chunk_attn_fp8_workspace_size(P, C, Hq, Hkv, d, d, 1) == 0
+    need = vpp.chunk_attn_fp8_workspace_size(P, C, Hq, Hkv, d, d, 3)
+    assert need >= 3 * C * Hq * (d + 1) * 4
+    assert vpp.chunk_attn_fp8_workspace_size(30 * P, C, Hq, Hkv, d, d, 3) == need
     k = gen((P + C, Hkv, d), 7, 0.1)
     cache = Fp8Cache(k, k, amax_scales(k), amax_scales(k), seed=1)
     q = gen((C, Hq, d), 8, 0.1).to(DEV)
     small = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
     with pytest.raises(vpp.VppError) as e:
         vpp.vpp_chunk_attn_fp8(q, cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table,
-                               workspace=small)
+                               num_splits=3, workspace=small)
     assert e.value.code == vpp.VPP_ERR_WORKSPACE
+    out = vpp.vpp_chunk_attn_fp8(q, cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table,
+                                 num_splits=1)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("qmul", [1e-5, 3000.0])
+def test_fp8_chunk_attention_with_extreme_query_scales(qmul):
+    # q is turned into f16 operands in the kernel: very small and very large
+    # (but f16-representable) queries must give the oracle's result.
+    P, C, Hq, Hkv, d = 700, 150, 8, 2, 128
+    q = (gen((C, Hq, d), 61, 1 / math.sqrt(d)).float() * qmul).to(torch.bfloat16)
+    k = gen((P + C, Hkv, d), 62, 1 / math.sqrt(d))
+    v = gen((P + C, Hkv, d), 63, 1 / math.sqrt(d))
+    ks, vs = amax_scales(k), amax_scales(v)
+    cache = Fp8Cache(k, v, ks, vs, seed=4)
+    lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+    out = vpp.vpp_chunk_attn_fp8(q.to(DEV), cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table,
+                                 lse=lse)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    kq = ofp8.dequantize_kv(ofp8.quantize_kv(k.float().numpy(), ks), ks)
+    vq = ofp8.dequantize_kv(ofp8.quantize_kv(v.float().numpy(), vs), vs)
+    ref, ref_lse = oracle.causal_chunk_attention(to_np64(q), kq, vq, P)
+    assert_close(to_np64(out), ref)
+    assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
+
+
+def test_fp8_query_outside_f16_range_is_reported():
+    P, C, Hq, Hkv, d = 200, 40, 4, 1, 64
+    q = gen((C, Hq, d), 71, 0.1)
+    q[5, 2, 7] = 1.0e5  # beyond f16's largest finite value
+    k = gen((P + C, Hkv, d), 72, 0.1)
+    cache = Fp8Cache(k, k, amax_scales(k), amax_scales(k), seed=5)
+    vpp.vpp_chunk_attn_fp8(q.to(DEV), cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == vpp.VPP_ERR_INVALID
+    assert vpp.vpp_last_device_status() == 0  # the report is read once
 
 
 # ----------------------------------------------------------------- mixed batch
 CTX = [1, 2, 15, 16, 17, 63, 64, 65, 1000, 1023, 1024, 1025, 2048, 3001]
 
 
-def _mixed(ctx, qlen, Hq, Hkv, d, seed, qmul=1.0):
+def _mixed(ctx, qlen, Hq, Hkv, d, seed, qmul=1.0, widen=False):
     B = len(ctx)
     cu = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
     need = [(int(c) + 63) // 64 for c in ctx]
@@ -272,7 +332,7 @@ def _mixed(ctx, qlen, Hq, Hkv, d, seed, qmul=1.0):
         q = (q.float() * qmul).to(torch.bfloat16)
     lse = torch.empty((Hq, int(cu[-1])), dtype=torch.float32, device=DEV)
     out = vpp.vpp_mixed_attn_fp8(q.to(DEV), kc, vc, ksd, vsd, torch.from_numpy(table).to(DEV), cu,
-                                 np.asarray(ctx, dtype=np.int32), lse=lse)
+                                 np.asarray(ctx, dtype=np.int32), lse=lse, widen=widen)
     torch.cuda.synchronize()
     assert vpp.vpp_last_device_status() == 0
     kq = [ofp8.dequantize_kv(ofp8.quantize_kv(x.float().numpy(), kscale), kscale) for x in ks_]
@@ -294,7 +354,8 @@ def test_fp8_decode_rows_with_extreme_query_scales(qmul):
     _mixed([1, 17, 1000, 2048, 3001], [1] * 5, 32, 8, 128, seed=5, qmul=qmul)
 
 
-def test_fp8_mixed_prefill_and_decode():
+@pytest.mark.parametrize("widen", [False, True])
+def test_fp8_mixed_prefill_and_decode(widen):
     ctx = [300, 700, 64, 129, 1, 2000, 513, 4100]
     qlen = [300, 128, 1, 1, 1, 1, 77, 1]
-    _mixed(ctx, qlen, 8, 2, 128, seed=77)
+    _mixed(ctx, qlen, 8, 2, 128, seed=77, widen=widen)
