@@ -365,6 +365,21 @@ size_t widen_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int 
   return round_up((size_t)rows * kv_heads * dq * 2, 256) + round_up((size_t)rows * kv_heads * dv * 2, 256);
 }
 
+// CTAs of the decode kernel in a mixed batch (0: one per work item).
+int mixed_decode_ctas(int num_sms, bool fp8, bool with_prefill) {
+  (void)num_sms;
+  (void)fp8;
+  (void)with_prefill;
+  return 0;
+}
+
+// CTAs of the top-k gather (0: one per work item).
+int topk_ctas(int num_sms, bool fp8) {
+  (void)num_sms;
+  (void)fp8;
+  return 0;
+}
+
 // Mixed micro-batch over a paged cache, bf16 or (fp8) E4M3 codes with
 // per-kv-head scales.  Decode rows read the codes directly.  Chunk-attention
 // segments of an fp8 cache read the codes directly as well (the fp8 kernel
@@ -510,7 +525,8 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
     dst = ds->side;
   }
   int err = VPP_OK;
-  if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms, dst) != cudaSuccess)
+  if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms,
+                              mixed_decode_ctas(ds->num_sms, fp8, n > 0), dst) != cudaSuccess)
     err = VPP_ERR_CUDA;
   if (fork && cudaEventRecord(ds->ev_join, ds->side) != cudaSuccess) err = VPP_ERR_CUDA;
   if (err == VPP_OK) {
@@ -625,7 +641,8 @@ int topk_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache,
   dp.topk_splits = (int32_t)S;
   dp.topk_prefix = P;
   dp.topk_tokens = C;
-  if (launch_decode(dp, (int)items, d, fp8, true, ds->num_sms, st) != cudaSuccess) return VPP_ERR_CUDA;
+  if (launch_decode(dp, (int)items, d, fp8, true, ds->num_sms, topk_ctas(ds->num_sms, fp8), st) != cudaSuccess)
+    return VPP_ERR_CUDA;
   return VPP_OK;
 }
 

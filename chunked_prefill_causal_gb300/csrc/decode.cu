@@ -9,7 +9,8 @@
 // mixed micro-batch.  The arithmetic is Eq. (1) of the VPP review (§2.2) for
 // a query at position ctx-1 that sees keys 0..ctx-1.
 //
-// Work item = (row, key range of split_tokens keys).  One CTA per item:
+// Work item = (row, key range of split_tokens keys).  A CTA takes one item,
+// or, when the launch caps the CTA count, every ctas-th item in turn:
 //   warp Hkv (last)   producer: for every 16-token step, one 1-D bulk copy of
 //                     the step's K rows and four of its V rows (16 tokens x
 //                     all kv heads are contiguous inside a 64-token block),
@@ -157,6 +158,59 @@ __device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t x) {
   return y;
 }
 
+// One work item: keys [t_begin, t_end) of a decode row (top-k: list entries
+// [t_begin, t_end) of a query token), range `split` of the row's n_splits.
+struct DecodeItem {
+  DecodeRow row;
+  int split, n_splits, t_begin, t_end, n_steps;
+  const int32_t* list;  // SP: the token's index row
+  int64_t pos;          // SP: the token's absolute position
+  bool skip;            // SP: the token's list is shorter than this range (no work, nothing written)
+};
+
+// `report`: the one thread that records a top-k list length out of range.
+template <bool SP>
+__device__ __forceinline__ DecodeItem decode_item(const DecodeParams& p, int item, bool report) {
+  DecodeItem it;
+  it.list = nullptr;
+  it.pos = 0;
+  it.skip = false;
+  if (SP) {
+    const int64_t i = item / p.topk_splits;
+    it.split = item - static_cast<int>(i * p.topk_splits);
+    int n = __ldg(p.topk_len + i);
+    if (n < 1 || n > p.topk) {
+      if (report && it.split == 0) record_status(p.status, kStatusInvalid);
+      n = 0;
+    }
+    it.row.b = 0;
+    it.row.q_row = static_cast<int32_t>(i);
+    it.row.ctx = n;
+    it.row.item0 = static_cast<int32_t>(i * p.topk_splits);
+    it.list = p.topk_idx + i * p.topk;
+    it.pos = p.topk_prefix + i;
+    it.n_splits = n > 0 ? (n + p.split_tokens - 1) / p.split_tokens : 1;
+    it.skip = it.split >= it.n_splits;
+  } else {
+    int lo = 0, hi = p.n_rows - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.rows[mid].item0 <= item) lo = mid; else hi = mid - 1;
+    }
+    it.row = p.rows[lo];
+    it.split = item - it.row.item0;
+    it.n_splits = (it.row.ctx + p.split_tokens - 1) / p.split_tokens;
+  }
+  it.t_begin = it.split * p.split_tokens;
+  it.t_end = min(it.row.ctx, it.t_begin + p.split_tokens);
+  it.n_steps = it.skip ? 0 : (it.t_end - it.t_begin + kStepTokens - 1) / kStepTokens;
+  return it;
+}
+
+// Persistent: CTA b takes items b, b + gridDim.x, ... in turn; each role
+// keeps its place in the stage ring from one item to the next, so that the
+// producer fills the ring with the next item's rows while the kv-head warps
+// finish the current one.
 template <int D, int G, bool F8, bool SP>
 __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ? 2 : 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -181,42 +235,6 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   uint32_t* step_valid = reinterpret_cast<uint32_t*>(bars + 17);  // SP: valid-entry mask per stage
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---------------------------------------------------------- work item
-  const int item = blockIdx.x;
-  DecodeRow row;
-  int split, n_splits, t_begin, t_end;
-  const int32_t* list = nullptr;  // SP: this token's index row
-  int64_t pos = 0;                // SP: this token's absolute position
-  if (SP) {
-    const int64_t i = item / p.topk_splits;
-    split = item - static_cast<int>(i * p.topk_splits);
-    int n = __ldg(p.topk_len + i);
-    if (n < 1 || n > p.topk) {
-      if (threadIdx.x == 0 && split == 0) record_status(p.status, kStatusInvalid);
-      n = 0;
-    }
-    row.b = 0;
-    row.q_row = static_cast<int32_t>(i);
-    row.ctx = n;
-    row.item0 = static_cast<int32_t>(i * p.topk_splits);
-    list = p.topk_idx + i * p.topk;
-    pos = p.topk_prefix + i;
-    n_splits = n > 0 ? (n + p.split_tokens - 1) / p.split_tokens : 1;
-    if (split >= n_splits) return;  // the token's list is shorter: no work, nothing written
-  } else {
-    int lo = 0, hi = p.n_rows - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.rows[mid].item0 <= item) lo = mid; else hi = mid - 1;
-    }
-    row = p.rows[lo];
-    split = item - row.item0;
-    n_splits = (row.ctx + p.split_tokens - 1) / p.split_tokens;
-  }
-  t_begin = split * p.split_tokens;
-  t_end = min(row.ctx, t_begin + p.split_tokens);
-  const int n_steps = (t_end - t_begin + kStepTokens - 1) / kStepTokens;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -246,6 +264,9 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     const bool is_v = c >= 16;
     int32_t key_a[4], blk_a[4], key_b[4];  // group g + 1: keys, table entries; group g + 2: keys
     int64_t row_c[4];                      // group g: source rows, -1 if invalid or past the range
+    int t_begin = 0, t_end = 0;     // the current item's range of list entries
+    const int32_t* list = nullptr;  // its token's index row
+    int64_t pos = 0;                // its token's absolute position
     auto load_keys = [&](int grp, int32_t (&k)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -278,59 +299,68 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
         row_c[j] = (e < t_end && valid) ? r : -1;
       }
     };
-    load_keys(0, key_a);
-    load_blocks(key_a, blk_a);
-    load_keys(1, key_b);
     int slot = 0;
     uint32_t phase = 0u;
     uint32_t filled = 0u, fill_phase = 0u;
     bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      if ((s & 7) == 0) {
-        resolve(s >> 3);
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const DecodeItem it = decode_item<SP>(p, item, false);
+      if (it.skip) continue;
+      t_begin = it.t_begin;
+      t_end = it.t_end;
+      list = it.list;
+      pos = it.pos;
+      const int n_steps = it.n_steps;
+      load_keys(0, key_a);
+      load_blocks(key_a, blk_a);
+      load_keys(1, key_b);
+      for (int s = 0; s < n_steps; ++s) {
+        if ((s & 7) == 0) {
+          resolve(s >> 3);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) key_a[j] = key_b[j];
-        load_blocks(key_a, blk_a);
-        load_keys((s >> 3) + 2, key_b);
-      }
-      const int t0 = t_begin + s * kStepTokens;
-      const int nt = min(kStepTokens, t_end - t0);
-      const int kq = (s & 7) >> 1;
-      const int64_t mine = kq == 0 ? row_c[0] : kq == 1 ? row_c[1] : kq == 2 ? row_c[2] : row_c[3];
-      // the step's validity word (lane l < 16: entry l), then this lane's row
-      const int64_t rl = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + (lane & 15));
-      const uint32_t vmask = __ballot_sync(0xffffffffu, lane < 16 && rl >= 0) & 0xFFFFu;
-      const int64_t src_row = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + t);
-      const bool mine_in = c < 32 && t < nt;
-      const bool valid = mine_in && ((vmask >> t) & 1u);
-      const uint32_t cmask = __ballot_sync(0xffffffffu, valid);
-      bool w_ok = true;
-      if (lane == 0) w_ok = mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag);
-      if (!__shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0)) {
-        ok = false;
-        break;
-      }
-      uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8, true>(t, kbytes, row_bytes) : t * kstride);
-      if (mine_in && !valid) {  // zero-filled, so that P = 0 times it stays 0
-        for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();  // before later bulk copies into these bytes
-      }
-      __syncwarp();
-      const uint32_t full = smem_u32(&bars[slot]);
-      if (lane == 0) {
-        if (gw == 0) step_valid[slot] = vmask;
-        mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(cmask)) * row_bytes);
-      }
-      __syncwarp();
-      if (valid) {
-        const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
-        bulk_g2s(smem_u32(dstp), base + src_row * row_bytes, static_cast<uint32_t>(row_bytes), full);
-      }
-      filled |= 1u << slot;
-      fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
-      if (++slot == nstage) {
-        slot = 0;
-        phase ^= 1u;
+          for (int j = 0; j < 4; ++j) key_a[j] = key_b[j];
+          load_blocks(key_a, blk_a);
+          load_keys((s >> 3) + 2, key_b);
+        }
+        const int t0 = t_begin + s * kStepTokens;
+        const int nt = min(kStepTokens, t_end - t0);
+        const int kq = (s & 7) >> 1;
+        const int64_t mine = kq == 0 ? row_c[0] : kq == 1 ? row_c[1] : kq == 2 ? row_c[2] : row_c[3];
+        // the step's validity word (lane l < 16: entry l), then this lane's row
+        const int64_t rl = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + (lane & 15));
+        const uint32_t vmask = __ballot_sync(0xffffffffu, lane < 16 && rl >= 0) & 0xFFFFu;
+        const int64_t src_row = __shfl_sync(0xffffffffu, mine, (s & 1) * 16 + t);
+        const bool mine_in = c < 32 && t < nt;
+        const bool valid = mine_in && ((vmask >> t) & 1u);
+        const uint32_t cmask = __ballot_sync(0xffffffffu, valid);
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag);
+        if (!__shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dstp = smem + slot * stage_bytes + (is_v ? v_row<F8, true>(t, kbytes, row_bytes) : t * kstride);
+        if (mine_in && !valid) {  // zero-filled, so that P = 0 times it stays 0
+          for (int b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dstp + b) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();  // before later bulk copies into these bytes
+        }
+        __syncwarp();
+        const uint32_t full = smem_u32(&bars[slot]);
+        if (lane == 0) {
+          if (gw == 0) step_valid[slot] = vmask;
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(cmask)) * row_bytes);
+        }
+        __syncwarp();
+        if (valid) {
+          const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
+          bulk_g2s(smem_u32(dstp), base + src_row * row_bytes, static_cast<uint32_t>(row_bytes), full);
+        }
+        filled |= 1u << slot;
+        fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
+        if (++slot == nstage) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!ok && lane == 0) {
@@ -344,37 +374,43 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
       uint32_t phase = 0u;
       uint32_t filled = 0u, fill_phase = 0u;
       bool ok = true;
-      for (int s = 0; s < n_steps; ++s) {
-        const int t0 = t_begin + s * kStepTokens;
-        const int nt = min(kStepTokens, t_end - t0);
-        int blk = p.block_table[static_cast<int64_t>(row.b) * p.max_blocks_per_seq + t0 / kBlockTokens];
-        if (blk < 0 || blk >= p.num_blocks) {
-          record_status(p.status, kStatusInvalid);
-          blk = -1;
-        }
-        if (!mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t full = smem_u32(&bars[slot]);
-        const uint32_t dst = smem_u32(smem + slot * stage_bytes);
-        if (blk >= 0) {
-          const int64_t off = (static_cast<int64_t>(blk) * kBlockTokens + t0 % kBlockTokens) * row_bytes;
-          const uint32_t bytes = static_cast<uint32_t>(nt * row_bytes);
-          mbar_arrive_expect_tx(full, 2 * bytes);
-          bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
-          const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
-          for (int g4 = 0; 4 * g4 < nt; ++g4)
-            bulk_g2s(dst + v_row<F8, false>(4 * g4, kbytes, row_bytes), vsrc + 4 * g4 * row_bytes,
-                     static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
-        } else {
-          mbar_arrive(full);  // invalid block: the step's rows are skipped
-        }
-        filled |= 1u << slot;
-        fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
-        if (++slot == nstage) {
-          slot = 0;
-          phase ^= 1u;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const DecodeItem it = decode_item<SP>(p, item, false);
+        if (it.skip) continue;
+        const DecodeRow row = it.row;
+        const int t_begin = it.t_begin, t_end = it.t_end, n_steps = it.n_steps;
+        for (int s = 0; s < n_steps; ++s) {
+          const int t0 = t_begin + s * kStepTokens;
+          const int nt = min(kStepTokens, t_end - t0);
+          int blk = p.block_table[static_cast<int64_t>(row.b) * p.max_blocks_per_seq + t0 / kBlockTokens];
+          if (blk < 0 || blk >= p.num_blocks) {
+            record_status(p.status, kStatusInvalid);
+            blk = -1;
+          }
+          if (!mbar_wait(smem_u32(&bars[8 + slot]), phase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars[slot]);
+          const uint32_t dst = smem_u32(smem + slot * stage_bytes);
+          if (blk >= 0) {
+            const int64_t off = (static_cast<int64_t>(blk) * kBlockTokens + t0 % kBlockTokens) * row_bytes;
+            const uint32_t bytes = static_cast<uint32_t>(nt * row_bytes);
+            mbar_arrive_expect_tx(full, 2 * bytes);
+            bulk_g2s(dst, static_cast<const uint8_t*>(p.k_cache) + off, bytes, full);
+            const uint8_t* vsrc = static_cast<const uint8_t*>(p.v_cache) + off;
+            for (int g4 = 0; 4 * g4 < nt; ++g4)
+              bulk_g2s(dst + v_row<F8, false>(4 * g4, kbytes, row_bytes), vsrc + 4 * g4 * row_bytes,
+                       static_cast<uint32_t>(min(4, nt - 4 * g4) * row_bytes), full);
+          } else {
+            mbar_arrive(full);  // invalid block: the step's rows are skipped
+          }
+          filled |= 1u << slot;
+          fill_phase = (fill_phase & ~(1u << slot)) | (phase << slot);
+          if (++slot == nstage) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
       if (!ok) {
@@ -407,250 +443,255 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     const int gq = lane >> 2;
     const int u = lane & 3;
     constexpr int KS = D / 16;  // k-steps of S, tiles of O
-    uint32_t qb[KS][2];
-    float qscale = 1.f;  // fp8: 2^-e of head gq
-    // bf16 top-k: lane u's 16-byte pieces of a row are pieces 4c + u (see the
-    // K reads); otherwise its D/4 elements are contiguous.
-    constexpr bool kInterleaved = SP && !F8;
-    const uint4* qrow = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D);
-    const uint4* qsrc = kInterleaved ? qrow + u : qrow + u * (D / 32);
-    if (!F8) {
-      // bf16 operands: q's pairs are the B fragment as they are.
-      uint32_t qw[D / 8];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        const uint4 w = gq < G ? __ldg(qsrc + (kInterleaved ? 4 * c : c)) : make_uint4(0u, 0u, 0u, 0u);
-        qw[4 * c] = w.x;
-        qw[4 * c + 1] = w.y;
-        qw[4 * c + 2] = w.z;
-        qw[4 * c + 3] = w.w;
-      }
-#pragma unroll
-      for (int s2 = 0; s2 < KS; ++s2) {
-        qb[s2][0] = qw[2 * s2];
-        qb[s2][1] = qw[2 * s2 + 1];
-      }
-    } else {
-      // f16 operands: q scaled per head by a power of two into f16's range.
-      float qv[D / 4];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
-        bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
-        bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
-        bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
-        bf16x2_to_f32(w.w, qv[8 * c + 6], qv[8 * c + 7]);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < D / 4; ++i) amax = fmaxf(amax, fabsf(qv[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      // 2^e puts the head's largest |q| in [2^14, 2^15): below f16's largest
-      // value, and every bf16 value of the head that is not negligible keeps
-      // its 8 significant bits.
-      const int e = amax > 0.f ? max(-60, min(60, 14 - ilogbf(amax))) : 0;
-      const float up = ldexpf(1.f, e);
-      qscale = ldexpf(1.f, -e);
-#pragma unroll
-      for (int s2 = 0; s2 < KS; ++s2) {
-        qb[s2][0] = pack_f16x2(qv[4 * s2] * up, qv[4 * s2 + 1] * up);
-        qb[s2][1] = pack_f16x2(qv[4 * s2 + 2] * up, qv[4 * s2 + 3] * up);
-      }
-    }
-    // This thread's S^T columns are heads 2u and 2u + 1.
-    const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
-    const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
-                          sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
-    const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
-    float m[2] = {-INFINITY, -INFINITY};
-    float lpart[2] = {0.f, 0.f};
-    float o[KS][4];
-#pragma unroll
-    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float* pw = pbuf + h * kStepTokens * 8;  // P of the step: [16 tokens][8 heads]
     int slot = 0;
     uint32_t phase = 0u;
     bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      const int t0 = t_begin + s * kStepTokens;
-      const int nt = min(kStepTokens, t_end - t0);
-      ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint8_t* kst = smem + slot * stage_bytes;
-      const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
-      // ---- S^T = K Q^T (two accumulator chains)
-      // A thread reads KW words (D/4 elements) of each of its two token rows.
-      // Decode rows lie a multiple of 128 bytes apart, so a quarter warp's
-      // two groups would hit the same banks: the 16-byte pieces are read in
-      // an order that depends on the lane (and put back in place by
-      // selects).  Top-k rows are copied one by one and padded instead (16
-      // bytes past such a multiple for fp8, 64 for bf16, whose lanes take
-      // interleaved pieces), and read in order: 7-12% faster top-k than the
-      // lane-dependent order.
-      constexpr int KW = D * ESZ / 16;  // 32-bit words of a thread's part of one K row
-      uint32_t kw[2][KW];
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const DecodeItem it = decode_item<SP>(p, item, threadIdx.x == 0);
+      if (it.skip) continue;  // the token's list is shorter: no work, nothing written
+      const DecodeRow row = it.row;
+      const int t_begin = it.t_begin, t_end = it.t_end, n_steps = it.n_steps, n_splits = it.n_splits;
+      uint32_t qb[KS][2];
+      float qscale = 1.f;  // fp8: 2^-e of head gq
+      // bf16 top-k: lane u's 16-byte pieces of a row are pieces 4c + u (see the
+      // K reads); otherwise its D/4 elements are contiguous.
+      constexpr bool kInterleaved = SP && !F8;
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D);
+      const uint4* qsrc = kInterleaved ? qrow + u : qrow + u * (D / 32);
+      if (!F8) {
+        // bf16 operands: q's pairs are the B fragment as they are.
+        uint32_t qw[D / 8];
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        uint4 w[KW / 4];
-        const uint4* src = reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * kstride +
-                                                          (h * D + (kInterleaved ? 0 : u * (D / 4))) * ESZ);
-        if (kInterleaved) {
-          // pieces 4c + u: the four lanes of a group read four consecutive
-          // 16-byte units, and rows 64 bytes past a multiple of 128 put the
-          // next group's row in the other half of the banks
-#pragma unroll
-          for (int c = 0; c < KW / 4; ++c) w[c] = src[4 * c + u];
-        } else if (KW / 4 == 4) {
-          const int r = SP ? 0 : (u >> 1) | ((gq & 1) << 1);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) w[c] = src[c ^ r];
-          // w[c] holds piece c ^ r: two conditional swaps put piece j in w[j]
-          if (r & 1) {
-            const uint4 t0 = w[0], t2 = w[2];
-            w[0] = w[1]; w[1] = t0; w[2] = w[3]; w[3] = t2;
-          }
-          if (r & 2) {
-            const uint4 t0 = w[0], t1 = w[1];
-            w[0] = w[2]; w[1] = w[3]; w[2] = t0; w[3] = t1;
-          }
-        } else if (KW / 4 == 2) {
-          const int sw = SP ? 0 : gq & 1;
-          const uint4 wa = src[sw], wb = src[sw ^ 1];
-          w[0] = sw ? wb : wa;
-          w[1 % (KW / 4)] = sw ? wa : wb;
-        } else {
-          w[0] = src[0];
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 w = gq < G ? __ldg(qsrc + (kInterleaved ? 4 * c : c)) : make_uint4(0u, 0u, 0u, 0u);
+          qw[4 * c] = w.x;
+          qw[4 * c + 1] = w.y;
+          qw[4 * c + 2] = w.z;
+          qw[4 * c + 3] = w.w;
         }
 #pragma unroll
-        for (int c = 0; c < KW / 4; ++c) {
-          kw[rr][4 * c] = w[c].x;
-          kw[rr][4 * c + 1] = w[c].y;
-          kw[rr][4 * c + 2] = w[c].z;
-          kw[rr][4 * c + 3] = w[c].w;
+        for (int s2 = 0; s2 < KS; ++s2) {
+          qb[s2][0] = qw[2 * s2];
+          qb[s2][1] = qw[2 * s2 + 1];
+        }
+      } else {
+        // f16 operands: q scaled per head by a power of two into f16's range.
+        float qv[D / 4];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+          bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
+          bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
+          bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
+          bf16x2_to_f32(w.w, qv[8 * c + 6], qv[8 * c + 7]);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // 2^e puts the head's largest |q| in [2^14, 2^15): below f16's largest
+        // value, and every bf16 value of the head that is not negligible keeps
+        // its 8 significant bits.
+        const int e = amax > 0.f ? max(-60, min(60, 14 - ilogbf(amax))) : 0;
+        const float up = ldexpf(1.f, e);
+        qscale = ldexpf(1.f, -e);
+#pragma unroll
+        for (int s2 = 0; s2 < KS; ++s2) {
+          qb[s2][0] = pack_f16x2(qv[4 * s2] * up, qv[4 * s2 + 1] * up);
+          qb[s2][1] = pack_f16x2(qv[4 * s2 + 2] * up, qv[4 * s2 + 3] * up);
         }
       }
-      float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // This thread's S^T columns are heads 2u and 2u + 1.
+      const float sl = F8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
+      const float slh[2] = {sl * __shfl_sync(0xffffffffu, qscale, 8 * u),
+                            sl * __shfl_sync(0xffffffffu, qscale, 8 * u + 4)};
+      const float vsc = F8 ? __ldg(p.v_scale + h) : 1.f;
+      float m[2] = {-INFINITY, -INFINITY};
+      float lpart[2] = {0.f, 0.f};
+      float o[KS][4];
 #pragma unroll
-      for (int s2 = 0; s2 < KS; ++s2) {
-        if (F8) {
-          uint32_t a0, a1, a2, a3;
-          e4m3x4_to_f16x2x2(kw[0][s2 % KW], a0, a2);
-          e4m3x4_to_f16x2x2(kw[1][s2 % KW], a1, a3);
-          mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
-        } else {
-          mma_16816_bf16(sa[s2 & 1], kw[0][(2 * s2) % KW], kw[1][(2 * s2) % KW], kw[0][(2 * s2 + 1) % KW],
-                         kw[1][(2 * s2 + 1) % KW], qb[s2][0], qb[s2][1]);
-        }
-      }
-      // sc[rr][hh]: token gq + 8 rr, head 2u + hh
-      float sc[2][2];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int t = gq + 8 * rr;
-        const bool tv = t < nt && ((vmask >> t) & 1u);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          sc[rr][hh] = (tv && 2 * u + hh < G) ? (sa[0][2 * rr + hh] + sa[1][2 * rr + hh]) * slh[hh] : -INFINITY;
-      }
-      // ---- online softmax per head (the 8 lanes of one u hold its 16 tokens)
-      float pvr[2][2];  // top-k: P of tokens gq, gq + 8 for heads 2u, 2u + 1
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float mx = fmaxf(sc[0][hh], sc[1][hh]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        if (mx > m[hh] + 8.0f || (m[hh] == -INFINITY && mx != -INFINITY)) {  // uniform over the 8 lanes
-          const float f = (m[hh] == -INFINITY) ? 0.f : ex2_approx(m[hh] - mx);
-          lpart[hh] *= f;
-#pragma unroll
-          for (int i = 0; i < KS; ++i) {
-            o[i][hh] *= f;
-            o[i][2 + hh] *= f;
-          }
-          m[hh] = mx;
-        }
+      for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int s = 0; s < n_steps; ++s) {
+        const int t0 = t_begin + s * kStepTokens;
+        const int nt = min(kStepTokens, t_end - t0);
+        ok = mbar_wait(smem_u32(&bars[slot]), phase, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint8_t* kst = smem + slot * stage_bytes;
+        const uint32_t vmask = SP ? step_valid[slot] : 0xFFFFu;
+        // ---- S^T = K Q^T (two accumulator chains)
+        // A thread reads KW words (D/4 elements) of each of its two token rows.
+        // Decode rows lie a multiple of 128 bytes apart, so a quarter warp's
+        // two groups would hit the same banks: the 16-byte pieces are read in
+        // an order that depends on the lane (and put back in place by
+        // selects).  Top-k rows are copied one by one and padded instead (16
+        // bytes past such a multiple for fp8, 64 for bf16, whose lanes take
+        // interleaved pieces), and read in order: 7-12% faster top-k than the
+        // lane-dependent order.
+        constexpr int KW = D * ESZ / 16;  // 32-bit words of a thread's part of one K row
+        uint32_t kw[2][KW];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-          const float pv = (m[hh] == -INFINITY) ? 0.f : ex2_approx(sc[rr][hh] - m[hh]);
-          lpart[hh] += pv;
-          if (SP) {
-            pvr[rr][hh] = pv;
+          uint4 w[KW / 4];
+          const uint4* src = reinterpret_cast<const uint4*>(kst + (gq + 8 * rr) * kstride +
+                                                            (h * D + (kInterleaved ? 0 : u * (D / 4))) * ESZ);
+          if (kInterleaved) {
+            // pieces 4c + u: the four lanes of a group read four consecutive
+            // 16-byte units, and rows 64 bytes past a multiple of 128 put the
+            // next group's row in the other half of the banks
+#pragma unroll
+            for (int c = 0; c < KW / 4; ++c) w[c] = src[4 * c + u];
+          } else if (KW / 4 == 4) {
+            const int r = SP ? 0 : (u >> 1) | ((gq & 1) << 1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) w[c] = src[c ^ r];
+            // w[c] holds piece c ^ r: two conditional swaps put piece j in w[j]
+            if (r & 1) {
+              const uint4 t0 = w[0], t2 = w[2];
+              w[0] = w[1]; w[1] = t0; w[2] = w[3]; w[3] = t2;
+            }
+            if (r & 2) {
+              const uint4 t0 = w[0], t1 = w[1];
+              w[0] = w[2]; w[1] = w[3]; w[2] = t0; w[3] = t1;
+            }
+          } else if (KW / 4 == 2) {
+            const int sw = SP ? 0 : gq & 1;
+            const uint4 wa = src[sw], wb = src[sw ^ 1];
+            w[0] = sw ? wb : wa;
+            w[1 % (KW / 4)] = sw ? wa : wb;
           } else {
-            pw[(gq + 8 * rr) * 8 + 2 * u + hh] = pv;
+            w[0] = src[0];
+          }
+#pragma unroll
+          for (int c = 0; c < KW / 4; ++c) {
+            kw[rr][4 * c] = w[c].x;
+            kw[rr][4 * c + 1] = w[c].y;
+            kw[rr][4 * c + 2] = w[c].z;
+            kw[rr][4 * c + 3] = w[c].w;
           }
         }
-      }
-      // ---- O^T += V^T P^T
-      uint32_t pb0, pb1;
-      if (SP) {
-        // P^T's B fragment is the transpose of P in the accumulator layout:
-        // tokens 2u, 2u + 1 (and + 8) of head gq after one 8x8 transpose each
-        pb0 = transpose8x8_b16(F8 ? pack_f16x2(pvr[0][0], pvr[0][1]) : pack_bf16x2(pvr[0][0], pvr[0][1]));
-        pb1 = transpose8x8_b16(F8 ? pack_f16x2(pvr[1][0], pvr[1][1]) : pack_bf16x2(pvr[1][0], pvr[1][1]));
-      } else {
+        float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int s2 = 0; s2 < KS; ++s2) {
+          if (F8) {
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(kw[0][s2 % KW], a0, a2);
+            e4m3x4_to_f16x2x2(kw[1][s2 % KW], a1, a3);
+            mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
+          } else {
+            mma_16816_bf16(sa[s2 & 1], kw[0][(2 * s2) % KW], kw[1][(2 * s2) % KW], kw[0][(2 * s2 + 1) % KW],
+                           kw[1][(2 * s2 + 1) % KW], qb[s2][0], qb[s2][1]);
+          }
+        }
+        // sc[rr][hh]: token gq + 8 rr, head 2u + hh
+        float sc[2][2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int t = gq + 8 * rr;
+          const bool tv = t < nt && ((vmask >> t) & 1u);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            sc[rr][hh] = (tv && 2 * u + hh < G) ? (sa[0][2 * rr + hh] + sa[1][2 * rr + hh]) * slh[hh] : -INFINITY;
+        }
+        // ---- online softmax per head (the 8 lanes of one u hold its 16 tokens)
+        float pvr[2][2];  // top-k: P of tokens gq, gq + 8 for heads 2u, 2u + 1
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float mx = fmaxf(sc[0][hh], sc[1][hh]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          if (mx > m[hh] + 8.0f || (m[hh] == -INFINITY && mx != -INFINITY)) {  // uniform over the 8 lanes
+            const float f = (m[hh] == -INFINITY) ? 0.f : ex2_approx(m[hh] - mx);
+            lpart[hh] *= f;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+              o[i][hh] *= f;
+              o[i][2 + hh] *= f;
+            }
+            m[hh] = mx;
+          }
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float pv = (m[hh] == -INFINITY) ? 0.f : ex2_approx(sc[rr][hh] - m[hh]);
+            lpart[hh] += pv;
+            if (SP) {
+              pvr[rr][hh] = pv;
+            } else {
+              pw[(gq + 8 * rr) * 8 + 2 * u + hh] = pv;
+            }
+          }
+        }
+        // ---- O^T += V^T P^T
+        uint32_t pb0, pb1;
+        if (SP) {
+          // P^T's B fragment is the transpose of P in the accumulator layout:
+          // tokens 2u, 2u + 1 (and + 8) of head gq after one 8x8 transpose each
+          pb0 = transpose8x8_b16(F8 ? pack_f16x2(pvr[0][0], pvr[0][1]) : pack_bf16x2(pvr[0][0], pvr[0][1]));
+          pb1 = transpose8x8_b16(F8 ? pack_f16x2(pvr[1][0], pvr[1][1]) : pack_bf16x2(pvr[1][0], pvr[1][1]));
+        } else {
+          __syncwarp();
+          pb0 = F8 ? pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq])
+                   : pack_bf16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
+          pb1 = F8 ? pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq])
+                   : pack_bf16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
+        }
+        // tokens 4u .. 4u + 3 (top-k: 2u, 2u + 1, 2u + 8, 2u + 9): this
+        // thread's D/8 elements of each
+        constexpr int VW = D * ESZ / 32;  // 32-bit words of them
+        uint32_t vw[4][VW];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int t = SP ? 2 * u + (q4 & 1) + 8 * (q4 >> 1) : 4 * u + q4;
+          const uint8_t* src = kst + v_row<F8, SP>(t, kbytes, row_bytes) + (h * D + gq * (D / 8)) * ESZ;
+          uint32_t w[VW];
+          if (VW == 8) {
+            const uint4 w0 = reinterpret_cast<const uint4*>(src)[0];
+            const uint4 w1 = reinterpret_cast<const uint4*>(src)[1];
+            w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+            w[4 % VW] = w1.x; w[5 % VW] = w1.y; w[6 % VW] = w1.z; w[7 % VW] = w1.w;
+          } else if (VW == 4) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+            w[0] = w0.x; w[1 % VW] = w0.y; w[2 % VW] = w0.z; w[3 % VW] = w0.w;
+          } else {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(src);
+            w[0] = w0.x; w[1 % VW] = w0.y;
+          }
+          // rows past the range hold stale bytes: zeros (P is 0 there)
+#pragma unroll
+          for (int c = 0; c < VW; ++c) vw[q4][c] = t < nt ? w[c] : 0u;
+        }
         __syncwarp();
-        pb0 = F8 ? pack_f16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq])
-                 : pack_bf16x2(pw[(4 * u) * 8 + gq], pw[(4 * u + 1) * 8 + gq]);
-        pb1 = F8 ? pack_f16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq])
-                 : pack_bf16x2(pw[(4 * u + 2) * 8 + gq], pw[(4 * u + 3) * 8 + gq]);
-      }
-      // tokens 4u .. 4u + 3 (top-k: 2u, 2u + 1, 2u + 8, 2u + 9): this
-      // thread's D/8 elements of each
-      constexpr int VW = D * ESZ / 32;  // 32-bit words of them
-      uint32_t vw[4][VW];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int t = SP ? 2 * u + (q4 & 1) + 8 * (q4 >> 1) : 4 * u + q4;
-        const uint8_t* src = kst + v_row<F8, SP>(t, kbytes, row_bytes) + (h * D + gq * (D / 8)) * ESZ;
-        uint32_t w[VW];
-        if (VW == 8) {
-          const uint4 w0 = reinterpret_cast<const uint4*>(src)[0];
-          const uint4 w1 = reinterpret_cast<const uint4*>(src)[1];
-          w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-          w[4 % VW] = w1.x; w[5 % VW] = w1.y; w[6 % VW] = w1.z; w[7 % VW] = w1.w;
-        } else if (VW == 4) {
-          const uint4 w0 = *reinterpret_cast<const uint4*>(src);
-          w[0] = w0.x; w[1 % VW] = w0.y; w[2 % VW] = w0.z; w[3 % VW] = w0.w;
-        } else {
-          const uint2 w0 = *reinterpret_cast<const uint2*>(src);
-          w[0] = w0.x; w[1 % VW] = w0.y;
+        for (int i = 0; i < KS; ++i) {
+          uint32_t a0, a1, a2, a3;
+          if (F8) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x = __byte_perm(vw[0][(i >> 1) % VW], vw[1][(i >> 1) % VW], sel);
+            const uint32_t y = __byte_perm(vw[2][(i >> 1) % VW], vw[3][(i >> 1) % VW], sel);
+            e4m3x4_to_f16x2x2(x, a0, a1);
+            e4m3x4_to_f16x2x2(y, a2, a3);
+            mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+          } else {
+            // word i of a token holds dims 2i, 2i + 1 of the thread's part
+            a0 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x5410u);
+            a1 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x7632u);
+            a2 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x5410u);
+            a3 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x7632u);
+            mma_16816_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
+          }
         }
-        // rows past the range hold stale bytes: zeros (P is 0 there)
-#pragma unroll
-        for (int c = 0; c < VW; ++c) vw[q4][c] = t < nt ? w[c] : 0u;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        uint32_t a0, a1, a2, a3;
-        if (F8) {
-          const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-          const uint32_t x = __byte_perm(vw[0][(i >> 1) % VW], vw[1][(i >> 1) % VW], sel);
-          const uint32_t y = __byte_perm(vw[2][(i >> 1) % VW], vw[3][(i >> 1) % VW], sel);
-          e4m3x4_to_f16x2x2(x, a0, a1);
-          e4m3x4_to_f16x2x2(y, a2, a3);
-          mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
-        } else {
-          // word i of a token holds dims 2i, 2i + 1 of the thread's part
-          a0 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x5410u);
-          a1 = __byte_perm(vw[0][i % VW], vw[1][i % VW], 0x7632u);
-          a2 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x5410u);
-          a3 = __byte_perm(vw[2][i % VW], vw[3][i % VW], 0x7632u);
-          mma_16816_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
+        if (++slot == nstage) {
+          slot = 0;
+          phase ^= 1u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[8 + slot]));
-      if (++slot == nstage) {
-        slot = 0;
-        phase ^= 1u;
-      }
-    }
-    if (ok) {
+      if (!ok) break;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float l = lpart[hh];
@@ -741,7 +782,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 }
 
 template <int D, int G, bool F8, bool SP>
-cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t st) {
+cudaError_t launch_t(const DecodeParams& p, int items, int ctas, int num_sms, cudaStream_t st) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -753,7 +794,10 @@ cudaError_t launch_t(const DecodeParams& p, int items, int num_sms, cudaStream_t
     configured[dev] = true;
   }
   const int warps = p.kv_heads + (SP ? gather_warps<F8>() : 1);
-  decode_kernel<D, G, F8, SP><<<items, 32 * warps, smem_bytes<F8>(), st>>>(p);
+  DecodeParams pk = p;
+  pk.n_items = items;
+  const int ctas_used = ctas > 0 ? std::min(items, ctas) : items;
+  decode_kernel<D, G, F8, SP><<<ctas_used, 32 * warps, smem_bytes<F8>(), st>>>(pk);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = SP ? p.topk_tokens : static_cast<int64_t>(p.n_rows);
@@ -773,29 +817,29 @@ bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads) 
 }
 
 template <bool F8, bool SP>
-cudaError_t launch_f(const DecodeParams& p, int items, int head_dim, int num_sms, cudaStream_t stream) {
+cudaError_t launch_f(const DecodeParams& p, int items, int head_dim, int num_sms, int ctas, cudaStream_t stream) {
   const int g = p.heads / p.kv_heads;
   if (head_dim == 128) {
-    if (g == 1) return launch_t<128, 1, F8, SP>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<128, 2, F8, SP>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<128, 4, F8, SP>(p, items, num_sms, stream);
-    if (g == 8) return launch_t<128, 8, F8, SP>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<128, 1, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 2) return launch_t<128, 2, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 4) return launch_t<128, 4, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 8) return launch_t<128, 8, F8, SP>(p, items, ctas, num_sms, stream);
   } else if (head_dim == 64) {
-    if (g == 1) return launch_t<64, 1, F8, SP>(p, items, num_sms, stream);
-    if (g == 2) return launch_t<64, 2, F8, SP>(p, items, num_sms, stream);
-    if (g == 4) return launch_t<64, 4, F8, SP>(p, items, num_sms, stream);
-    if (g == 8) return launch_t<64, 8, F8, SP>(p, items, num_sms, stream);
+    if (g == 1) return launch_t<64, 1, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 2) return launch_t<64, 2, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 4) return launch_t<64, 4, F8, SP>(p, items, ctas, num_sms, stream);
+    if (g == 8) return launch_t<64, 8, F8, SP>(p, items, ctas, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, bool topk, int num_sms,
-                          cudaStream_t stream) {
+                          int ctas, cudaStream_t stream) {
   if (topk)
-    return fp8 ? launch_f<true, true>(p, items, head_dim, num_sms, stream)
-               : launch_f<false, true>(p, items, head_dim, num_sms, stream);
-  return fp8 ? launch_f<true, false>(p, items, head_dim, num_sms, stream)
-             : launch_f<false, false>(p, items, head_dim, num_sms, stream);
+    return fp8 ? launch_f<true, true>(p, items, head_dim, num_sms, ctas, stream)
+               : launch_f<false, true>(p, items, head_dim, num_sms, ctas, stream);
+  return fp8 ? launch_f<true, false>(p, items, head_dim, num_sms, ctas, stream)
+             : launch_f<false, false>(p, items, head_dim, num_sms, ctas, stream);
 }
 
 }  // namespace vpp

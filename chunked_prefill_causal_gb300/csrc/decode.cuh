@@ -24,7 +24,7 @@ struct DecodeParams {
   int32_t num_blocks;
   int32_t max_blocks_per_seq;
   float scale_log2;
-  int32_t pad0;
+  int32_t n_items;             // work items of the launch (set by launch_decode)
   const uint16_t* q;           // bf16 [total_q][heads][d]
   const void* k_cache;         // [num_blocks][64][kv_heads][d], bf16 or E4M3 codes
   const void* v_cache;
@@ -58,7 +58,10 @@ bool decode_supported(int head_dim_qk, int head_dim_v, int heads, int kv_heads);
 
 // fp8: the cache holds E4M3 codes with per-kv-head k_scale / v_scale.
 // topk: p.topk_idx rows instead of decode rows (items = tokens x topk_splits).
+// ctas > 0: at most that many CTAs, each taking every ctas-th item (one
+// resident CTA per SM on a bf16 cache, two on an fp8 one); 0: one CTA per
+// item.
 cudaError_t launch_decode(const DecodeParams& p, int items, int head_dim, bool fp8, bool topk, int num_sms,
-                          cudaStream_t stream);
+                          int ctas, cudaStream_t stream);
 
 }  // namespace vpp
