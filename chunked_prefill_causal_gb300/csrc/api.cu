@@ -70,7 +70,11 @@ int device_state(DeviceState** out) {
         return VPP_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess ||
+    // Highest priority: when the decode kernel runs on a share of the SMs,
+    // its CTAs are placed before the prefill CTAs launched after it.
+    int prio_lo = 0, prio_hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, prio_hi) != cudaSuccess ||
         cudaEventCreateWithFlags(&s.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&s.ev_join, cudaEventDisableTiming) != cudaSuccess)
       return VPP_ERR_CUDA;
@@ -365,12 +369,31 @@ size_t widen_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int 
   return round_up((size_t)rows * kv_heads * dq * 2, 256) + round_up((size_t)rows * kv_heads * dv * 2, 256);
 }
 
-// CTAs of the decode kernel in a mixed batch (0: one per work item).
-int mixed_decode_ctas(int num_sms, bool fp8, bool with_prefill) {
-  (void)num_sms;
-  (void)fp8;
-  (void)with_prefill;
-  return 0;
+// Measured rates that split the SMs of a mixed batch: one decode CTA reads
+// about 80 GB/s of a bf16 cache (two fp8 CTAs share an SM, about 40 GB/s of
+// codes each); a prefill CTA does about 9.9 TFLOP/s on one SM with bf16
+// operands, about 4.1 reading E4M3 codes (widened in shared memory).
+constexpr double kDecodeSmGBs = 80.0;
+constexpr double kPrefillSmTFlops = 9.9;
+constexpr double kPrefillSmTFlopsF8 = 4.1;
+
+// CTAs of the decode kernel in a mixed batch (0: one per work item).  The
+// decode rows are HBM-bound and the prefill segments tensor-bound, but a
+// kernel that starts first takes every SM.  So the decode kernel runs on a
+// fixed share of the SMs, the one where both would finish together, and the
+// prefill CTAs fill the rest (and the decode's SMs once it is done).  The
+// share is rounded up by 10%: a decode that ends last leaves SMs idle, and
+// the step time is flat over a range of shares around the best one.  A batch
+// without prefill segments, or whose decode needs nearly every SM anyway,
+// runs one CTA per work item.
+int mixed_decode_ctas(int num_sms, bool fp8, double prefill_flops, double decode_bytes, bool f8_prefill) {
+  if (prefill_flops <= 0.0 || decode_bytes <= 0.0 || num_sms < 2) return 0;
+  const double f = f8_prefill ? kPrefillSmTFlopsF8 : kPrefillSmTFlops;
+  const double r = (decode_bytes * f * 1e12) / (prefill_flops * kDecodeSmGBs * 1e9);
+  const double sms = 1.1 * num_sms * r / (1.0 + r);
+  if (sms >= 0.9 * num_sms) return 0;
+  const int d = std::max(1, (int)std::ceil(sms));
+  return fp8 ? 2 * d : d;
 }
 
 // CTAs of the top-k gather (0: one per work item).
@@ -509,11 +532,11 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
   }
 
   // The decode rows (HBM-bound) are launched first, on the side stream, and
-  // the prefill segments (tensor-bound) on the caller's stream: the two
-  // kernels' CTAs share the SMs instead of running one after the other.
-  // They write disjoint rows of out / lse and disjoint workspace.  (Measured
-  // on the 256-row mixed batch: -1% on a bf16 cache, -5% on an fp8 one; a
-  // highest-priority side stream gained nothing.)
+  // the prefill segments (tensor-bound) on the caller's stream, so that the
+  // two kernels' CTAs share the SMs instead of running one after the other:
+  // the decode kernel on the share mixed_decode_ctas gives it, the prefill
+  // CTAs on the rest.  They write disjoint rows of out / lse and disjoint
+  // workspace.
   std::unique_lock<std::mutex> side_lock(ds->side_mutex, std::defer_lock);
   cudaStream_t dst = st;
   const bool fork = nd > 0 && n > 0;
@@ -525,8 +548,16 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
     dst = ds->side;
   }
   int err = VPP_OK;
-  if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms,
-                              mixed_decode_ctas(ds->num_sms, fp8, n > 0), dst) != cudaSuccess)
+  double prefill_flops = 0.0, decode_bytes = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const double c = cu_seqlens_q[order[i] + 1] - cu_seqlens_q[order[i]];
+    const double pre = ctx_lens[order[i]] - c;
+    prefill_flops += 2.0 * (head_dim_qk + head_dim_v) * heads * (c * pre + c * (c + 1) / 2);
+  }
+  for (int i = 0; i < nd; ++i)
+    decode_bytes += (double)ctx_lens[drows[i]] * kv_heads * (head_dim_qk + head_dim_v) * (fp8 ? 1 : 2);
+  const int dctas = mixed_decode_ctas(ds->num_sms, fp8, prefill_flops, decode_bytes, fp8 && !widen);
+  if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms, dctas, dst) != cudaSuccess)
     err = VPP_ERR_CUDA;
   if (fork && cudaEventRecord(ds->ev_join, ds->side) != cudaSuccess) err = VPP_ERR_CUDA;
   if (err == VPP_OK) {

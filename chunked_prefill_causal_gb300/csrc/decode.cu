@@ -47,6 +47,7 @@
 // pool, are zero-filled, masked out of the softmax and reported as
 // VPP_ERR_INVALID.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "decode.cuh"
@@ -236,6 +237,13 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // The ring starts zeroed.  A short step copies only its valid rows, so the
+  // rows past them hold rows of an earlier step (finite cache values) or
+  // zeros, and their P = 0 adds exactly nothing: the V fragments need no
+  // mask.  (The fence orders these writes before the ring's bulk copies.)
+  for (int i = threadIdx.x; i < kRing / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     for (int i = 0; i < nstage; ++i) {
@@ -447,25 +455,55 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
     int slot = 0;
     uint32_t phase = 0u;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-      const DecodeItem it = decode_item<SP>(p, item, threadIdx.x == 0);
+    // bf16 top-k: lane u's 16-byte pieces of a row are pieces 4c + u (see the
+    // K reads); otherwise its D/4 elements are contiguous.
+    constexpr bool kInterleaved = SP && !F8;
+    // This lane's bf16 q words of an item (query head h G + gq; zeros for
+    // gq >= G).  With a capped CTA count the next item's words are loaded
+    // while the current item runs, so that an item starts without waiting
+    // for them (fp8, two CTAs per SM, has no registers to spare for it).
+    constexpr bool kPrefetchQ = !F8;
+    auto load_q = [&](const DecodeItem& x, uint4 (&w)[D / 32]) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(x.row.q_row) * p.heads + h * G + min(gq, G - 1)) * D);
+      const uint4* qsrc = kInterleaved ? qrow + u : qrow + u * (D / 32);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+        w[c] = (gq < G && !x.skip) ? __ldg(qsrc + (kInterleaved ? 4 * c : c)) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    int item = blockIdx.x;
+    DecodeItem it_next;
+    uint4 q_next[D / 32];
+    if (kPrefetchQ && item < p.n_items) {
+      it_next = decode_item<SP>(p, item, threadIdx.x == 0);
+      load_q(it_next, q_next);
+    }
+    for (; ok && item < p.n_items; item += gridDim.x) {
+      DecodeItem it;
+      uint4 q_cur[D / 32];
+      if (kPrefetchQ) {
+        it = it_next;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) q_cur[c] = q_next[c];
+        if (item + static_cast<int>(gridDim.x) < p.n_items) {
+          it_next = decode_item<SP>(p, item + gridDim.x, threadIdx.x == 0);
+          load_q(it_next, q_next);
+        }
+      } else {
+        it = decode_item<SP>(p, item, threadIdx.x == 0);
+        load_q(it, q_cur);
+      }
       if (it.skip) continue;  // the token's list is shorter: no work, nothing written
       const DecodeRow row = it.row;
       const int t_begin = it.t_begin, t_end = it.t_end, n_steps = it.n_steps, n_splits = it.n_splits;
       uint32_t qb[KS][2];
       float qscale = 1.f;  // fp8: 2^-e of head gq
-      // bf16 top-k: lane u's 16-byte pieces of a row are pieces 4c + u (see the
-      // K reads); otherwise its D/4 elements are contiguous.
-      constexpr bool kInterleaved = SP && !F8;
-      const uint4* qrow = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(row.q_row) * p.heads + h * G + min(gq, G - 1)) * D);
-      const uint4* qsrc = kInterleaved ? qrow + u : qrow + u * (D / 32);
       if (!F8) {
         // bf16 operands: q's pairs are the B fragment as they are.
         uint32_t qw[D / 8];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          const uint4 w = gq < G ? __ldg(qsrc + (kInterleaved ? 4 * c : c)) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w = q_cur[c];
           qw[4 * c] = w.x;
           qw[4 * c + 1] = w.y;
           qw[4 * c + 2] = w.z;
@@ -481,7 +519,7 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
         float qv[D / 4];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          const uint4 w = gq < G ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w = q_cur[c];
           bf16x2_to_f32(w.x, qv[8 * c + 0], qv[8 * c + 1]);
           bf16x2_to_f32(w.y, qv[8 * c + 2], qv[8 * c + 3]);
           bf16x2_to_f32(w.z, qv[8 * c + 4], qv[8 * c + 5]);
@@ -573,17 +611,29 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
             kw[rr][4 * c + 3] = w[c].w;
           }
         }
-        float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // NCH independent accumulator chains (bf16: four, 4% faster than two;
+        // fp8, two CTAs per SM, keeps two for registers), summed after.
+        constexpr int NCH = (F8 || KS < 4) ? 2 : 4;
+        float sa[NCH][4];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) sa[j][0] = sa[j][1] = sa[j][2] = sa[j][3] = 0.f;
 #pragma unroll
         for (int s2 = 0; s2 < KS; ++s2) {
           if (F8) {
             uint32_t a0, a1, a2, a3;
             e4m3x4_to_f16x2x2(kw[0][s2 % KW], a0, a2);
             e4m3x4_to_f16x2x2(kw[1][s2 % KW], a1, a3);
-            mma_16816(sa[s2 & 1], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
+            mma_16816(sa[s2 % NCH], a0, a1, a2, a3, qb[s2][0], qb[s2][1]);
           } else {
-            mma_16816_bf16(sa[s2 & 1], kw[0][(2 * s2) % KW], kw[1][(2 * s2) % KW], kw[0][(2 * s2 + 1) % KW],
+            mma_16816_bf16(sa[s2 % NCH], kw[0][(2 * s2) % KW], kw[1][(2 * s2) % KW], kw[0][(2 * s2 + 1) % KW],
                            kw[1][(2 * s2 + 1) % KW], qb[s2][0], qb[s2][1]);
+          }
+        }
+        if (NCH == 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sa[0][e] += sa[2 % NCH][e];
+            sa[1][e] += sa[3 % NCH][e];
           }
         }
         // sc[rr][hh]: token gq + 8 rr, head 2u + hh
@@ -660,9 +710,8 @@ __global__ void __launch_bounds__(SP ? 32 * (8 + gather_warps<F8>()) : 288, F8 ?
             const uint2 w0 = *reinterpret_cast<const uint2*>(src);
             w[0] = w0.x; w[1 % VW] = w0.y;
           }
-          // rows past the range hold stale bytes: zeros (P is 0 there)
 #pragma unroll
-          for (int c = 0; c < VW; ++c) vw[q4][c] = t < nt ? w[c] : 0u;
+          for (int c = 0; c < VW; ++c) vw[q4][c] = w[c];
         }
         __syncwarp();
 #pragma unroll
@@ -794,6 +843,8 @@ cudaError_t launch_t(const DecodeParams& p, int items, int ctas, int num_sms, cu
     configured[dev] = true;
   }
   const int warps = p.kv_heads + (SP ? gather_warps<F8>() : 1);
+  // item + gridDim.x stays below 2^31 in the kernels' item loops
+  if (items < 0 || items > INT32_MAX / 2) return cudaErrorInvalidValue;
   DecodeParams pk = p;
   pk.n_items = items;
   const int ctas_used = ctas > 0 ? std::min(items, ctas) : items;
