@@ -396,12 +396,11 @@ int mixed_decode_ctas(int num_sms, bool fp8, double prefill_flops, double decode
   return fp8 ? 2 * d : d;
 }
 
-// CTAs of the top-k gather (0: one per work item).
-int topk_ctas(int num_sms, bool fp8) {
-  (void)num_sms;
-  (void)fp8;
-  return 0;
-}
+// CTAs of the top-k gather (0: one per work item).  Over a bf16 cache one
+// persistent CTA per SM keeps each CTA's gather pipeline running from one
+// item to the next: 2.5-6% faster on dsa128k's chunks.  Over an fp8 cache
+// (two CTAs per SM) a capped grid measured no faster.
+int topk_ctas(int num_sms, bool fp8) { return fp8 ? 0 : num_sms; }
 
 // Mixed micro-batch over a paged cache, bf16 or (fp8) E4M3 codes with
 // per-kv-head scales.  Decode rows read the codes directly.  Chunk-attention
