@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "3cec2b28afee8f0f61f13d505c3c25f3a3c93159502ee6da68e33ac373b0d239", "bytes_per_launch": 1.222e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "b8b5f2523980c0d2691b6e6c0615c8bc2733181e7cef65189fd34734eeca4f85", "bytes_per_launch": 1.210e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 
