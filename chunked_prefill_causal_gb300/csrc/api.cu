@@ -7,7 +7,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "chunk_attn.cuh"
 #include "common.cuh"
@@ -168,53 +170,182 @@ int make_contig_map_u8(CUtensorMap* m, const void* cache, int64_t n_tokens, int 
   return encode_map_u8(m, cache, 3, dims, strides, box);
 }
 
-struct SplitPlan {
+int pairs_for(int64_t q_len, int group) { return (int)ceil_div(q_len, 2 * (kTileM / group)); }
+
+// Work plan of one chunk (a7).  Query tokens [t0, C) form the heavy group,
+// launched first, whose key range [0, P + t0 + i] is cut into n_splits
+// ranges of split_keys keys (the last range takes the rest); tokens [0, t0)
+// form the light group, unsplit.  t0 = 0: a single group.
+struct ChunkPlan {
+  int t0;
   int n_splits;
   int split_keys;
 };
 
-int pairs_for(int64_t q_len, int group) { return (int)ceil_div(q_len, 2 * (kTileM / group)); }
+// Key ranges of a group whose tokens sit after P_seg cached keys: S requested
+// ranges of whole 128-key tiles, fewer when the prefix is short.
+ChunkPlan uniform_plan(int64_t P_seg, int S, int t0) {
+  if (S <= 1 || P_seg < kTileN) return ChunkPlan{t0, 1, 0};
+  S = std::min(S, 16);
+  const int64_t keys = round_up((size_t)ceil_div(P_seg, S), (size_t)kTileN);
+  const int64_t S_eff = std::min<int64_t>(S, P_seg / keys + 1);
+  if (S_eff <= 1) return ChunkPlan{t0, 1, 0};
+  return ChunkPlan{t0, (int)S_eff, (int)keys};
+}
 
-// Chooses the number of key ranges for one chunk.  The model: a CTA costs its
-// key count plus a fixed ~256 keys of prologue/epilogue; CTAs run in waves of
-// num_sms; a split adds a float32 round trip of the partials through HBM.
-SplitPlan plan_splits(int64_t P, int64_t C, int heads, int kv_heads, int dv, int requested,
-                      int num_sms) {
-  SplitPlan none{1, 0};
-  if (requested == 1 || P < kTileN || C <= 0) return none;
-  const int G = heads / kv_heads;
-  const int64_t base = (int64_t)pairs_for(C, G) * kv_heads;
-  int S = requested;
-  if (requested <= 0) {
-    const double key_ns = 8.5;  // one key of one CTA (two 128-row tiles, d = 128)
-    double best = 1e300;
-    S = 1;
-    for (int s = 1; s <= 16; ++s) {
-      if (s > 1 && P / s < 512) break;
-      const double waves = std::ceil((double)(base * s) / num_sms);
-      double t = waves * ((double)P / s + 0.5 * C + 256.0) * key_ns;
-      if (s > 1) t += (double)(s + 1) * C * heads * dv * 4.0 / 5.0e3;  // ns at ~5 TB/s
-      if (t < best * 0.98) {
-        best = t;
-        S = s;
+// Cost model of a launch, fitted on GB300 to 55 timed gqa32k chunks (1 to 8
+// key ranges for every token, or 2 for the heaviest eighth; 1.7% rms error,
+// 5% at most): CTAs start in launch order on the first free SM (list
+// scheduling); a CTA costs 12.5 ns per key of its range (whole 128-key tiles;
+// d_qk + d_v = 256) plus 8 us of prologue and epilogue, 2 us more when it
+// writes float32 partials; the merge kernel that follows a split costs 8 us
+// plus its partials read at 6 TB/s.
+constexpr double kKeyNs = 12.5;
+constexpr double kCtaNs = 8000.0;
+constexpr double kSplitCtaNs = 2000.0;
+constexpr double kMergeNs = 8000.0;
+constexpr double kMergeBytesPerNs = 6000.0;
+
+double predict_ns(const ChunkPlan& pl, int64_t P, int64_t C, int G, int kv_heads, int dq, int dv,
+                  int num_sms, std::vector<double>& heap, double give_up = 1e300) {
+  const double key_ns = kKeyNs * (dq + dv) / 256.0;
+  const int T2 = 2 * (kTileM / G);
+  heap.assign(num_sms, 0.0);  // min-heap of SM free times
+  double* h = heap.data();
+  const int n = num_sms;
+  double span = 0.0;  // latest SM free time so far: a lower bound of the result
+  // The next CTA goes to the SM that frees first: add its cost to the root
+  // and sift the root down.
+  auto take = [&](double c) {
+    const double v = h[0] + c;
+    int i = 0;
+    while (true) {
+      int k = 2 * i + 1;
+      if (k >= n) break;
+      if (k + 1 < n && h[k + 1] < h[k]) ++k;
+      if (h[k] >= v) break;
+      h[i] = h[k];
+      i = k;
+    }
+    h[i] = v;
+    span = std::max(span, v);
+  };
+  for (int grp = 0; grp < 2; ++grp) {
+    const int64_t a = grp == 0 ? pl.t0 : 0, b = grp == 0 ? C : pl.t0;
+    if (b <= a) continue;
+    const int S = grp == 0 ? pl.n_splits : 1;
+    const int64_t P_seg = P + a, q = b - a;
+    const int np = pairs_for(q, G);
+    // CTA costs of one kv head in launch order (the same for every kv head).
+    thread_local std::vector<double> cost;
+    cost.clear();
+    for (int r = 0; r < np; ++r) {
+      const int pair = np - 1 - r;
+      const int64_t hi = P_seg + std::min<int64_t>((int64_t)(pair + 1) * T2, q);
+      for (int sp = 0; sp < S; ++sp) {
+        const int64_t lo = (int64_t)sp * pl.split_keys;
+        const int64_t end = sp == S - 1 ? hi : lo + pl.split_keys;
+        cost.push_back((double)ceil_div(end - lo, kTileN) * kTileN * key_ns + kCtaNs + (S > 1 ? kSplitCtaNs : 0.0));
       }
     }
+    for (int g = 0; g < kv_heads; ++g) {
+      for (double c : cost) take(c);
+      if (span > give_up) return span;  // already worse than the plan to beat
+    }
   }
-  S = std::min(S, 16);
-  if (S <= 1) return none;
-  const int64_t keys = round_up((size_t)ceil_div(P, S), (size_t)kTileN);
-  const int64_t S_eff = std::min<int64_t>(S, P / keys + 1);
-  if (S_eff <= 1) return none;
-  return SplitPlan{(int)S_eff, (int)keys};
+  if (pl.n_splits <= 1) return span;
+  const double merge_bytes = (double)pl.n_splits * (C - pl.t0) * G * kv_heads * (dv + 1) * 4.0;
+  return span + kMergeNs + merge_bytes / kMergeBytesPerNs;
+}
+
+struct PlanKey {
+  int64_t P, C;
+  int heads, kv_heads, dq, dv, requested, num_sms;
+  bool operator==(const PlanKey& o) const {
+    return P == o.P && C == o.C && heads == o.heads && kv_heads == o.kv_heads && dq == o.dq && dv == o.dv &&
+           requested == o.requested && num_sms == o.num_sms;
+  }
+};
+std::mutex g_plan_mutex;
+PlanKey g_plan_keys[64];
+ChunkPlan g_plans[64];
+int g_plan_count = 0;
+
+// Chooses the plan.  An explicit request of S ranges splits every query token
+// the same way.  Otherwise, when the chunk is a few waves of CTAs, the model
+// above picks between uniform plans (1 to 8 ranges) and plans whose heaviest
+// query-tile pairs alone take 2 to 4 ranges, filling the last wave without
+// paying the splitting costs on every CTA; a split plan must beat the unsplit
+// one by 2%.  Plans are remembered per shape (the choice costs up to ~1 ms of
+// host time for a new shape).
+ChunkPlan plan_chunk(int64_t P, int64_t C, int heads, int kv_heads, int dq, int dv, int requested,
+                     int num_sms) {
+  if (requested >= 1 || C <= 0) return uniform_plan(P, requested, 0);
+  const int G = heads / kv_heads;
+  const int np = pairs_for(C, G);
+  const int64_t base = (int64_t)np * kv_heads;
+  if (base >= 6LL * num_sms || num_sms < 1) return ChunkPlan{0, 1, 0};
+  const PlanKey key{P, C, heads, kv_heads, dq, dv, requested, num_sms};
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    for (int i = 0; i < std::min(g_plan_count, 64); ++i)
+      if (g_plan_keys[i] == key) return g_plans[i];
+  }
+  std::vector<double> heap;
+  const int T2 = 2 * (kTileM / G);
+  ChunkPlan best{0, 1, 0};
+  const double t1 = predict_ns(best, P, C, G, kv_heads, dq, dv, num_sms, heap);
+  double best_t = t1;
+  auto consider = [&](const ChunkPlan& pl) {
+    if (pl.n_splits <= 1) return;
+    const double t = predict_ns(pl, P, C, G, kv_heads, dq, dv, num_sms, heap, std::min(best_t, 0.98 * t1));
+    if (t < best_t && t < 0.98 * t1) {
+      best_t = t;
+      best = pl;
+    }
+  };
+  for (int S = 2; S <= 8; ++S)
+    if (base * S <= 8LL * num_sms && P / S >= 512) consider(uniform_plan(P, S, 0));
+  // The h heaviest pairs of every kv head split into S ranges: h on a grid
+  // of np/8, and the counts that bring the CTAs just under whole waves.
+  for (int S = 2; S <= 3; ++S) {
+    std::vector<int> hs;
+    for (int h = std::max(1, np / 8); h < np; h += std::max(1, np / 8)) hs.push_back(h);
+    for (int64_t w = (base + num_sms - 1) / num_sms; w <= (base + num_sms - 1) / num_sms + 2; ++w) {
+      const int64_t h0 = (w * num_sms - base) / ((int64_t)kv_heads * (S - 1));
+      for (int64_t h = h0 - 1; h <= h0 + 1; ++h)
+        if (h >= 1 && h < np) hs.push_back((int)h);
+    }
+    for (int h : hs) {
+      const int t0 = (np - h) * T2;
+      consider(uniform_plan(P + t0, S, t0));
+    }
+  }
+  std::lock_guard<std::mutex> lock(g_plan_mutex);
+  g_plan_keys[g_plan_count % 64] = key;
+  g_plans[g_plan_count % 64] = best;
+  ++g_plan_count;
+  return best;
 }
 
 size_t ws_q_bytes(int q_dtype, int64_t C, int heads, int dq) {
   return q_dtype == VPP_FP32 ? round_up((size_t)C * heads * dq * 2, 256) : 0;
 }
 
-size_t ws_split_bytes(int S, int64_t C, int heads, int dv) {
-  if (S <= 1) return 0;
-  return round_up((size_t)S * C * heads * dv * 4, 256) + round_up((size_t)S * C * heads * 4, 256);
+// Workspace of a plan's split group: float32 partial outputs, then their
+// LSEs, of its n_splits x (C - t0) token rows.
+struct SplitWs {
+  size_t o_bytes, lse_bytes;
+  size_t total() const { return o_bytes + lse_bytes; }
+};
+
+SplitWs ws_split(const ChunkPlan& pl, int64_t C, int heads, int dv) {
+  SplitWs w{0, 0};
+  if (pl.n_splits <= 1) return w;
+  const size_t rows = (size_t)pl.n_splits * (C - pl.t0);
+  w.o_bytes = round_up(rows * heads * dv * 4, 256);
+  w.lse_bytes = round_up(rows * heads * 4, 256);
+  return w;
 }
 
 int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
@@ -241,9 +372,10 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   DeviceState* ds = nullptr;
   if (int r = device_state(&ds)) return r;
 
-  const SplitPlan sp = plan_splits(P, C, heads, kv_heads, dv, num_splits, ds->num_sms);
+  const ChunkPlan pl = plan_chunk(P, C, heads, kv_heads, dq, dv, num_splits, ds->num_sms);
   const size_t need_q = ws_q_bytes(q_dtype, C, heads, dq);
-  const size_t need_s = ws_split_bytes(sp.n_splits, C, heads, dv);
+  const SplitWs sw = ws_split(pl, C, heads, dv);
+  const size_t need_s = sw.total();
   if (need_q + need_s > 0 && (!workspace || ws_bytes < need_q + need_s || !aligned16(workspace)))
     return VPP_ERR_WORKSPACE;
 
@@ -274,7 +406,7 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
 
   static AttnParams zero_params;  // value-initialised template
   AttnParams p = zero_params;
-  p.n_segs = 1;
+  p.n_segs = 0;
   p.heads = heads;
   p.kv_heads = kv_heads;
   p.group = heads / kv_heads;
@@ -288,26 +420,35 @@ int chunk_attn_impl(const void* q, int q_dtype, const void* k_cache, const void*
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.status = ds->status;
-  if (sp.n_splits > 1) {
-    p.ws_o = reinterpret_cast<float*>(ws + need_q);
-    p.ws_lse = reinterpret_cast<float*>(ws + need_q + round_up((size_t)sp.n_splits * C * heads * dv * 4, 256));
+  // Segment 0: the heavy group (query tokens [t0, C), n_splits key ranges,
+  // launched first); segment 1: the light group (tokens [0, t0), unsplit).
+  int grid = 0;
+  for (int grp = 0; grp < 2; ++grp) {
+    const int64_t a = grp == 0 ? pl.t0 : 0, b = grp == 0 ? C : pl.t0;
+    if (b <= a) continue;
+    AttnSeg& s = p.segs[p.n_segs++];
+    s.q_start = (int32_t)a;
+    s.q_len = (int32_t)(b - a);
+    s.kv_len = (int32_t)(P + b);
+    s.table_off = 0;
+    s.kv_base = 0;
+    s.n_pairs = pairs_for(b - a, p.group);
+    s.n_splits = grp == 0 ? pl.n_splits : 1;
+    s.split_keys = s.n_splits > 1 ? pl.split_keys : 0;
+    s.cta_begin = grid;
+    s.ws_row0 = 0;
+    const int64_t ctas = (int64_t)s.n_pairs * kv_heads * s.n_splits;
+    if (grid + ctas > INT32_MAX) return VPP_ERR_INVALID;
+    grid += (int)ctas;
   }
-  AttnSeg& s = p.segs[0];
-  s.q_start = 0;
-  s.q_len = (int32_t)C;
-  s.kv_len = (int32_t)(P + C);
-  s.table_off = 0;
-  s.n_pairs = pairs_for(C, p.group);
-  s.n_splits = sp.n_splits;
-  s.split_keys = sp.n_splits > 1 ? sp.split_keys : 0;
-  s.cta_begin = 0;
-  s.ws_row0 = 0;
-  const int64_t grid = (int64_t)s.n_pairs * kv_heads * s.n_splits;
-  if (grid > INT32_MAX) return VPP_ERR_INVALID;
-  if (launch_chunk_attn(dq, dv, f8, tm_q, tm_k, tm_v, p, (int)grid, st) != cudaSuccess)
-    return VPP_ERR_CUDA;
-  if (sp.n_splits > 1) {
-    if (launch_lse_merge(p.ws_o, p.ws_lse, 0, sp.n_splits, (int)C, 0, heads, dv,
+  if (pl.n_splits > 1) {
+    p.ws_o = reinterpret_cast<float*>(ws + need_q);
+    p.ws_lse = reinterpret_cast<float*>(ws + need_q + sw.o_bytes);
+  }
+  if (launch_chunk_attn(dq, dv, f8, tm_q, tm_k, tm_v, p, grid, st) != cudaSuccess) return VPP_ERR_CUDA;
+  if (pl.n_splits > 1) {
+    // the heavy group's rows: tokens [t0, C)
+    if (launch_lse_merge(p.ws_o, p.ws_lse, 0, pl.n_splits, (int)(C - pl.t0), pl.t0, heads, dv,
                          static_cast<uint16_t*>(out), lse, C, ds->num_sms, st) != cudaSuccess)
       return VPP_ERR_CUDA;
   }
@@ -781,26 +922,35 @@ int vpp_chunk_attn_ex(const void* q, int q_dtype, const void* k_cache, const voi
                          num_splits, out, lse, workspace, workspace_bytes, as_stream(stream));
 }
 
-int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
-                              int head_dim_qk, int head_dim_v, int num_splits) {
+int vpp_chunk_attn_plan(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads, int head_dim_qk,
+                        int head_dim_v, int num_splits, int64_t* split_token) {
   if (prefix_len < 0 || chunk_len < 0 || num_splits < 0) return VPP_ERR_INVALID;
   if (int r = check_heads(heads, kv_heads)) return r;
   if (!supported_dims(head_dim_qk, head_dim_v)) return VPP_ERR_UNSUPPORTED;
   DeviceState* ds = nullptr;
   int num_sms = 152;
   if (device_state(&ds) == VPP_OK) num_sms = ds->num_sms;
-  return plan_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_v, num_splits, num_sms)
-      .n_splits;
+  const ChunkPlan pl = plan_chunk(prefix_len, chunk_len, heads, kv_heads, head_dim_qk, head_dim_v, num_splits,
+                                  num_sms);
+  if (split_token) *split_token = pl.n_splits > 1 ? pl.t0 : 0;
+  return pl.n_splits;
+}
+
+int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len, int heads, int kv_heads,
+                              int head_dim_qk, int head_dim_v, int num_splits) {
+  return vpp_chunk_attn_plan(prefix_len, chunk_len, heads, kv_heads, head_dim_qk, head_dim_v, num_splits,
+                             nullptr);
 }
 
 size_t vpp_chunk_attn_workspace_size(int q_dtype, int64_t prefix_len, int64_t chunk_len,
                                      int heads, int kv_heads, int head_dim_qk, int head_dim_v,
                                      int num_splits) {
-  const int S = vpp_chunk_attn_num_splits(prefix_len, chunk_len, heads, kv_heads, head_dim_qk,
-                                          head_dim_v, num_splits);
+  int64_t t0 = 0;
+  const int S = vpp_chunk_attn_plan(prefix_len, chunk_len, heads, kv_heads, head_dim_qk, head_dim_v,
+                                    num_splits, &t0);
   if (S < 1) return 0;
   return ws_q_bytes(q_dtype, chunk_len, heads, head_dim_qk) +
-         ws_split_bytes(S, chunk_len, heads, head_dim_v);
+         ws_split(ChunkPlan{(int)t0, S, 0}, chunk_len, heads, head_dim_v).total();
 }
 
 int vpp_mixed_attn(const void* q, const void* k_cache, const void* v_cache,

@@ -37,6 +37,7 @@ SIGNATURES = {
                                 _int, _int, _f32, _int, _c_void_p, _c_void_p, _c_void_p], _int),
     "vpp_chunk_attn_workspace_size": ([_int, _i64, _i64, _int, _int, _int, _int, _int], _sz),
     "vpp_chunk_attn_num_splits": ([_i64, _i64, _int, _int, _int, _int, _int], _int),
+    "vpp_chunk_attn_plan": ([_i64, _i64, _int, _int, _int, _int, _int, ctypes.POINTER(_i64)], _int),
     "vpp_mixed_attn": ([_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
                         _i32, _int, _int, _int, _int, _f32, _c_void_p, _c_void_p, _c_void_p, _sz,
                         _c_void_p], _int),
@@ -186,6 +187,16 @@ def chunk_attn_workspace_size(q_dtype, prefix_len, chunk_len, heads, kv_heads, d
 def chunk_attn_num_splits(prefix_len, chunk_len, heads, kv_heads, dq, dv, num_splits=0):
     return int(load().vpp_chunk_attn_num_splits(int(prefix_len), int(chunk_len), heads, kv_heads,
                                                 dq, dv, num_splits))
+
+
+def chunk_attn_plan(prefix_len, chunk_len, heads, kv_heads, dq, dv, num_splits=0):
+    """(key ranges S, first query token whose keys are split) of the plan
+    vpp_chunk_attn_ex uses; raises on an invalid shape."""
+    t0 = _i64(0)
+    s = int(load().vpp_chunk_attn_plan(int(prefix_len), int(chunk_len), heads, kv_heads, dq, dv, num_splits,
+                                       ctypes.byref(t0)))
+    _check("vpp_chunk_attn_plan", VPP_OK if s >= 1 else s)
+    return s, int(t0.value)
 
 
 def vpp_chunk_attn_ex(q, k_cache, v_cache, prefix_len, block_table=None, out=None, lse=None,

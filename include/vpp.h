@@ -126,9 +126,12 @@ int vpp_chunk_attn(const void *q, const void *k_cache, const void *v_cache,
  * pool; contiguous otherwise, num_blocks = capacity in tokens, which must be
  * >= prefix_len + chunk_len).
  * num_splits: 0 lets the library choose; 1 forbids splitting; S > 1 asks
- * for S key ranges over the prefix (clamped so every range is non-empty).
- * With more than one range, each range writes a float32 partial (output,
- * lse) into the workspace and a merge kernel combines them
+ * for S key ranges over the prefix of every query token (clamped so every
+ * range is non-empty).  The library's own choice may split only the query
+ * tokens from some split token on (the heaviest query tiles, launched first),
+ * leaving the earlier ones unsplit; vpp_chunk_attn_plan reports it.  With more
+ * than one range, each range writes a float32 partial (output, lse) into the
+ * workspace and a merge kernel combines the split tokens' partials
  * ([GLM PP note] §7):  L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) out_s.
  * workspace: device scratch of at least vpp_chunk_attn_workspace_size(...)
  * bytes for the same arguments (NULL allowed when that size is 0).
@@ -180,6 +183,19 @@ size_t vpp_chunk_attn_workspace_size(int q_dtype, int64_t prefix_len,
                                      int64_t chunk_len, int heads,
                                      int kv_heads, int head_dim_qk,
                                      int head_dim_v, int num_splits);
+
+/*
+ * The work plan vpp_chunk_attn_ex uses for these arguments: returns the
+ * number of key ranges S (>= 1) or a negative status, and, if split_token is
+ * not NULL, stores the first query token whose keys are split (0: every
+ * token, or none when S = 1).  Tokens before it run unsplit.  Host-side; the
+ * library's choice ([VPP review] §2.3: a chunk's cost grows with its prefix)
+ * follows a list-scheduling model of the launch fitted on GB300 and is
+ * remembered per shape.
+ */
+int vpp_chunk_attn_plan(int64_t prefix_len, int64_t chunk_len, int heads,
+                        int kv_heads, int head_dim_qk, int head_dim_v,
+                        int num_splits, int64_t *split_token);
 
 /* The number of key ranges vpp_chunk_attn_ex will use for these arguments. */
 int vpp_chunk_attn_num_splits(int64_t prefix_len, int64_t chunk_len,

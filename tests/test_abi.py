@@ -130,6 +130,32 @@ def test_split_plan_is_host_side(lib):
     assert vpp.chunk_attn_workspace_size(vpp.VPP_FP32, 0, 64, 8, 8, 128, 128, 1) == 64 * 8 * 128 * 2
 
 
+def test_plan_splits_heavy_query_tiles_only(lib):
+    """The library's own plan for a gqa32k chunk (32/8 heads, C 4096, 512
+    unsplit CTAs = 3.4 waves of 152) splits the keys of the heaviest query
+    tiles only; an explicit request splits every token.  The workspace holds
+    exactly the split group's float32 partials and LSEs, each part rounded to
+    256 bytes."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    H, Hkv, d, C = 32, 8, 128, 4096
+    assert vpp.chunk_attn_plan(0, C, H, Hkv, d, d) == (1, 0)
+    for k in range(3, 8):
+        S, t0 = vpp.chunk_attn_plan(k * C, C, H, Hkv, d, d)
+        assert S >= 2 and 0 < t0 < C and t0 % 64 == 0
+        rows = S * (C - t0)
+        want = r256(rows * H * d * 4) + r256(rows * H * 4)
+        assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, k * C, C, H, Hkv, d, d) == want
+        assert vpp.chunk_attn_num_splits(k * C, C, H, Hkv, d, d) == S
+    assert vpp.chunk_attn_plan(5 * C, C, H, Hkv, d, d, num_splits=4) == (4, 0)
+    assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, 5 * C, C, H, Hkv, d, d, 4) == \
+        r256(4 * C * H * d * 4) + r256(4 * C * H * 4)
+    # many waves of CTAs (long128k: 4096 per chunk) are never split
+    assert vpp.chunk_attn_plan(7 * 16384, 16384, 64, 8, d, d) == (1, 0)
+    with pytest.raises(vpp.VppError):
+        vpp.chunk_attn_plan(0, C, 32, 5, d, d)
+
+
 def test_noalloc_host_checks_run_before_any_device_call(lib):
     null = None
     fake = ctypes.c_void_p(0x100000)  # never dereferenced

@@ -153,6 +153,50 @@ def test_split_prefix_matches_and_is_deterministic(splits):
     assert ma <= 2e-2 and rl <= 5e-3
 
 
+# Shapes where the library's own plan splits the keys of its heaviest query
+# tiles only: tokens from the split token on take S ranges, earlier tokens
+# none.  Hq, Hkv, d, P, C, expected (S, split token) on a 152-SM GB300.
+HEAVY_SPLIT = [
+    (32, 8, 128, 4096, 1536, (3, 1152)),
+    (16, 16, 64, 6000, 3072, (3, 2304)),   # G = 1
+]
+
+
+@pytest.mark.parametrize("case", HEAVY_SPLIT, ids=lambda c: "H%d-%d_d%d_P%d_C%d" % c[:5])
+def test_auto_plan_splitting_heavy_query_tiles(case):
+    """The heavy query tiles' key ranges are merged by the merge kernel; the
+    light tiles are written directly by the attention kernel.  Both match the
+    oracle row by row, repeat bit for bit, and the light rows equal the
+    unsplit kernel's bit for bit."""
+    Hq, Hkv, d, P, C, expect = case
+    assert vpp.chunk_attn_plan(P, C, Hq, Hkv, d, d) == expect
+    S, t0 = expect
+    assert t0 % (2 * 128 // (Hq // Hkv)) == 0
+    rows = S * (C - t0)
+    assert vpp.chunk_attn_workspace_size(vpp.VPP_BF16, P, C, Hq, Hkv, d, d) >= rows * Hq * (d + 1) * 4
+    q, k, v = make_seq(P + C, Hq, Hkv, d, d, seed=P + C + Hkv)
+    cache = Cache(k, v, True, seed=5)
+    qd = q[P:].to(DEV)
+
+    def run(num_splits):
+        lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+        out = vpp.vpp_chunk_attn_ex(qd, cache.k, cache.v, P, block_table=cache.table, lse=lse,
+                                    num_splits=num_splits)
+        torch.cuda.synchronize()
+        assert vpp.vpp_last_device_status() == 0
+        return out, lse
+
+    out, lse = run(0)
+    out2, lse2 = run(0)
+    base, base_lse = run(1)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    # the light tokens run the unsplit kernel's arithmetic
+    assert torch.equal(out[:t0], base[:t0]) and torch.equal(lse[:, :t0], base_lse[:, :t0])
+    ref, ref_lse = oracle.causal_chunk_attention(to_np64(q[P:]), to_np64(k), to_np64(v), P)
+    assert_close(to_np64(out), ref)
+    assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
+
+
 def test_zero_query_gives_running_mean_mask_probe():
     """Q = 0 and V[j, c] = bit c of j: the exact output is the running mean,
     so an off-by-one causal mask shows at O(1/p) at every tile boundary."""
