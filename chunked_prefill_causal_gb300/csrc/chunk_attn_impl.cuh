@@ -121,10 +121,11 @@ struct Shape {
   static constexpr int KP0 = 16 * PV0;  // keys of the first part
   static constexpr bool SPLIT_P = PV0 < kTileN / 16;  // PV0 = 8: one chain
   static_assert(PV0 >= 1 && PV0 <= kTileN / 16, "P V chain split out of range");
-  // barrier indices: Q, S[2], P0[2], O[2], FINAL[2], TMP, P1[2], FULL[NB], EMPTY[NB],
+  // barrier indices: Q, S[2], P0[2], O[2], FINAL[2], TMP, P1[2], END, FULL[NB], EMPTY[NB],
   // STAGE[NSTG]
   static constexpr int B_Q = 0, B_S = 1, B_P = 3, B_O = 5, B_FINAL = 7, B_TMP = 9, B_P1 = 10,
-                       B_FULL = 12, B_EMPTY = 12 + NB, B_STG = 12 + 2 * NB, NBARS = 12 + 2 * NB + NSTG;
+                       B_END = 12, B_FULL = 13, B_EMPTY = 13 + NB, B_STG = 13 + 2 * NB,
+                       NBARS = 13 + 2 * NB + NSTG;
   static_assert(NSLOT >= NQC + NVC, "ring must hold one K and one V tile");
   // With d_qk = 192 the ring holds under two K/V tile pairs, and the next K
   // tile can only start once V_{j-1} is free: V_{j-1} is released by its own
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(S::B_FINAL + x), 1);
     }
     mbar_init(bar(S::B_TMP), 1);
+    mbar_init(bar(S::B_END), 10);  // the 8 softmax warps and the 2 MMA issuers
     for (int i = 0; i < S::NB; ++i) {
       // over an fp8 cache a tile is full once each of its sub-tiles is widened
       // (K tiles, even t, use even barriers)
@@ -793,9 +795,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
 
-  tc_fence_before();
-  __syncthreads();
+  // TMEM is freed once the warps that use it are done: the softmax warps
+  // (tcgen05.ld/st; they have waited for their tile's last MMA) and the two
+  // MMA issuers (in the abort path after their MMAs have completed).  An
+  // mbarrier rather than a CTA barrier: the warps of the TMA/MMA warpgroup
+  // reach this point with lane 0 from a long role loop and the other lanes
+  // from none, and bar.sync there was measured to release them before the
+  // softmax warps had arrived; their other lanes, and the TMA producer (whose
+  // copies have all landed), just leave.  Warp 2 waits, bounded beyond every
+  // other wait, and frees TMEM.
+  if (warp >= 4) {
+    __syncwarp();
+    tc_fence_before();
+    if (lane == 0) mbar_arrive(bar(S::B_END));
+  } else if ((warp == 1 || warp == 3) && lane == 0) {
+    tc_fence_before();
+    mbar_arrive(bar(S::B_END));
+  }
   if (warp == 2) {
+    mbar_wait_for(bar(S::B_END), 0, 2 * kWaitTimeoutNs + 2 * kCleanupNs);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
