@@ -466,6 +466,50 @@ def measure_chunks(dev, stream, name, chunk_ids, peak_tf, peak_burst, iters):
             "frac_burst": round(tf / peak_burst, 4)}
 
 
+def measure_cpu_full(dev, stream, gqa_rows):
+    """Whole-chunk oracle times (fp64 NumPy on this host's cores) beside the
+    GPU's, for the chunks small enough to run in full within the bench: every
+    tiny chunk (fp32 inputs, contiguous cache) and gqa32k chunks 0 and 1; the
+    other configs' CPU times are extrapolated from the sampled rate.  The
+    inputs are the GPU run's, copied to the host.  Rows: [k, prefix, chunk,
+    GPU ms, oracle s]."""
+    import oracle
+    from chunked_prefill_causal_gb300 import vpp
+    out = {"cores": host_cores(), "columns": ["k", "prefix", "chunk", "gpu_ms", "oracle_s"], "tiny": [],
+           "gqa32k": []}
+    w = W.WORKLOADS["tiny"]
+    kc = torch.zeros((w.seq_len, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros((w.seq_len, w.kv_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    ks, vs = [], []
+    for ci, (P, C) in enumerate(w.chunks()):
+        q, k, v = W.chunk_tensors(w, ci, dev)
+        vpp.vpp_kv_append(k, v, kc, vc, P)
+        ks.append(k.cpu())
+        vs.append(v.cpu())
+        ws = torch.empty(max(256, vpp.chunk_attn_workspace_size(vpp.VPP_FP32, P, C, w.heads, w.kv_heads,
+                                                                w.head_dim_qk, w.head_dim_v)),
+                         dtype=torch.uint8, device=dev)
+        out_t = torch.empty((C, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+        t_gpu = time_events(lambda: vpp.vpp_chunk_attn_ex(q, kc, vc, P, out=out_t, workspace=ws), 20, stream)
+        qh = q.cpu().double().numpy()
+        kh, vh = torch.cat(ks).double().numpy(), torch.cat(vs).double().numpy()
+        t0 = time.perf_counter()
+        oracle.causal_chunk_attention(qh, kh, vh, P)
+        out["tiny"].append([ci, P, C, round(t_gpu, 4), round(time.perf_counter() - t0, 4)])
+    w = W.WORKLOADS["gqa32k"]
+    gpu_ms = {r[0]: r[3] for r in gqa_rows}
+    for ci in (0, 1):
+        P, C = w.chunks()[ci]
+        qh = W.chunk_tensors(w, ci, dev)[0].cpu().double().numpy()
+        kk, vv = W.sequence_kv(w, P + C, dev)
+        kh, vh = kk.cpu().double().numpy(), vv.cpu().double().numpy()
+        del kk, vv
+        t0 = time.perf_counter()
+        oracle.causal_chunk_attention(qh, kh, vh, P)
+        out["gqa32k"].append([ci, P, C, gpu_ms.get(ci), round(time.perf_counter() - t0, 2)])
+    return out
+
+
 def measure_append(dev, stream, hbm):
     """One MLA-chunk-sized append: 24576 tokens x 128 kv heads x (192 + 128) bf16."""
     from chunked_prefill_causal_gb300 import vpp
@@ -998,6 +1042,8 @@ def run_ours(args, dist_):
         extras["mla512k"] = measure_chunks(dev, stream, "mla512k", [0, 10, 20, 21], peak_tf, peak_tf_burst, 3)
         torch.cuda.empty_cache()
         extras["kv_append"] = measure_append(dev, stream, hbm)
+        if not args.no_cpu_baseline:
+            extras["cpu_full"] = measure_cpu_full(dev, stream, extras["gqa32k"]["rows"])
         extras["mixed"] = measure_mixed(dev, stream, hbm, peak_tf)
         torch.cuda.empty_cache()
         extras["cost_model"] = measure_cost_model(dev, stream)
@@ -1070,6 +1116,10 @@ def summary(line, peak_burst):
     if line.get("cpu_baseline"):
         out["cpu_tflops"] = r4(line["cpu_baseline"]["value"])
         out["cpu_cores"] = line["cpu_baseline"]["cores"]
+    cf = line.get("cpu_full")
+    if cf:
+        # whole-chunk oracle seconds: tiny chunks 0..3, gqa32k chunks 0 and 1
+        out["cpu_full_s"] = {"tiny": [r[4] for r in cf["tiny"]], "gqa32k": [r[4] for r in cf["gqa32k"]]}
     return out
 
 
