@@ -230,6 +230,15 @@ def test_fp8_split_prefix_matches(splits):
     run_fp8(2000, 100, 8, 2, 128, 128, seed=41, num_splits=splits)
 
 
+def test_fp8_heavy_query_tiles_split_by_the_library():
+    # The library's own plan for this shape splits only the keys of the tokens
+    # from 1152 on (3 ranges); over an E4M3 cache the codes are widened inside
+    # the kernel for both segments, and the merge covers the split tokens.
+    P, C, Hq, Hkv, d = 4096, 1536, 32, 8, 128
+    assert vpp.chunk_attn_plan(P, C, Hq, Hkv, d, d) == (3, 1152)
+    run_fp8(P, C, Hq, Hkv, d, d, seed=61)
+
+
 @pytest.mark.parametrize("case", [(640, 37, 8, 2, 128, 128, True, 0), (700, 129, 4, 4, 192, 128, True, 3),
                                   (250, 90, 4, 2, 192, 64, False, 0)],
                          ids=["d128_paged", "d192_paged_split3", "d192-64_contig"])

@@ -109,3 +109,23 @@ def test_noalloc_lowers_the_library_split_choice_to_fit_its_array():
         assert vpp.vpp_last_device_status() == 0
         assert torch.equal(got, ref)
         assert torch.equal(lse_b, lse_a)
+
+
+def test_noalloc_runs_the_library_heavy_tile_plan():
+    # The library's own plan for this shape splits only the keys of the tokens
+    # from 1152 on (3 ranges, 19 MB of partials): the allocation-free call runs
+    # that same plan in its array and matches the workspace entry point bit
+    # for bit, and both match the oracle.
+    Hq, Hkv, d, P, C = 32, 8, 128, 4096, 1536
+    assert vpp.chunk_attn_plan(P, C, Hq, Hkv, d, d) == (3, 1152)
+    q, kc, vc, table, (qh, kh, vh) = _case(Hq, Hkv, d, P, C, 24, host=True)
+    lse_a = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+    lse_b = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+    ref = vpp.vpp_chunk_attn_ex(q, kc, vc, P, block_table=table, lse=lse_a)
+    got = vpp.vpp_chunk_attn_noalloc(q, kc, vc, P, block_table=table, lse=lse_b)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    assert torch.equal(got, ref) and torch.equal(lse_b, lse_a)
+    want, want_lse = oracle.causal_chunk_attention(to_np64(qh), to_np64(kh), to_np64(vh), P)
+    assert_close(to_np64(got), want)
+    assert np.abs(to_np64(lse_b) - want_lse).max() <= LSE_ABS
