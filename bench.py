@@ -419,12 +419,14 @@ def time_flushed(fn, iters, stream, flush):
     return statistics.median(times)
 
 
-def measure_chunks(dev, stream, name, chunk_ids, peak_tf, peak_burst, iters):
+def measure_chunks(dev, stream, name, chunk_ids, peak_tf, peak_burst, iters, warm=False):
     """Chunk attention of chosen chunks of a workload, each timed in isolation
     (L2 flushed before every run) with the K/V of all earlier chunks and its
     own already in the paged cache, through the product call with the
     library's own split choice.  Rows: [k, prefix, chunk, ms, TFLOP/s,
-    fraction of the sustained peak, fraction of the burst peak]."""
+    fraction of the sustained peak, fraction of the burst peak], and with
+    warm=True an 8th column: the median ms of back-to-back runs without the
+    flush (whatever of the chunk's inputs L2 still holds)."""
     from chunked_prefill_causal_gb300 import vpp
     w = W.WORKLOADS[name]
     chunks = w.chunks()
@@ -455,13 +457,17 @@ def measure_chunks(dev, stream, name, chunk_ids, peak_tf, peak_burst, iters):
                                                        workspace=ws), iters, stream, flush)
         tf = chunk_flops(w, P, C) / (t / 1e3) / 1e12
         rows.append([ci, P, C, round(t, 3), round(tf, 1), round(tf / peak_tf, 4), round(tf / peak_burst, 4)])
+        if warm:
+            rows[-1].append(round(time_events(lambda: vpp.vpp_chunk_attn_ex(
+                qs[ci], kc, vc, P, block_table=table, out=out[:C], workspace=ws), iters, stream), 3))
     if vpp.vpp_last_device_status() != 0:
         raise RuntimeError(f"device status word reported an error during the {name} chunks")
     tot_f = sum(chunk_flops(w, r[1], r[2]) for r in rows)
     tot_ms = sum(r[3] for r in rows)
     tf = tot_f / (tot_ms / 1e3) / 1e12
     return {"workload": name, "heads": [w.heads, w.kv_heads], "head_dims": [w.head_dim_qk, w.head_dim_v],
-            "l2": "flushed before each run", "columns": ["k", "prefix", "chunk", "ms", "tflops", "frac", "frac_burst"],
+            "l2": "flushed before each run" + ("; ms_warm without the flush" if warm else ""),
+            "columns": ["k", "prefix", "chunk", "ms", "tflops", "frac", "frac_burst"] + (["ms_warm"] if warm else []),
             "rows": rows, "tflops": round(tf, 1), "frac": round(tf / peak_tf, 4),
             "frac_burst": round(tf / peak_burst, 4)}
 
@@ -1037,7 +1043,7 @@ def run_ours(args, dist_):
     if not args.no_extras:
         del qs, ks, vs
         torch.cuda.empty_cache()
-        extras["gqa32k"] = measure_chunks(dev, stream, "gqa32k", None, peak_tf, peak_tf_burst, 10)
+        extras["gqa32k"] = measure_chunks(dev, stream, "gqa32k", None, peak_tf, peak_tf_burst, 10, warm=True)
         torch.cuda.empty_cache()
         extras["mla512k"] = measure_chunks(dev, stream, "mla512k", [0, 10, 20, 21], peak_tf, peak_tf_burst, 3)
         torch.cuda.empty_cache()
