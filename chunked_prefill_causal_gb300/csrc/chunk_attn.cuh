@@ -54,10 +54,13 @@ constexpr int kAttnThreads = 384;  // warp 0 TMA, warps 1/3 MMA, warp 2 TMEM, WG
 constexpr int kSmemLimit = 232448; // 227 KB per CTA on sm_103a
 constexpr int kSubTileBytes = kTileN * 64 * 2;  // 128 keys x 64 bf16 (one 128B-swizzled block)
 
-// fp8 (E4M3) cache: the codes of one sub-tile (128 keys x 64 dims, one byte
-// each) land in a staging slot first and are widened into a ring slot.
-constexpr int kStageBytes = kTileN * 64;
-constexpr int kNumStages = 4;
+// fp8 (E4M3) cache: the codes of one half sub-tile (64 keys = one cache
+// block x 64 dims, one byte each) land in a staging slot first and are
+// widened into a ring slot; two staging slots per converter warp.
+constexpr int kStageBytes = kBlockTokens * 64;
+constexpr int kNumStages = 8;
+// Threads of a CTA: over an fp8 cache a fourth warpgroup widens the codes.
+__host__ __device__ constexpr int attn_threads(bool f8) { return f8 ? 512 : kAttnThreads; }
 
 __host__ __device__ constexpr int attn_q_bytes(int dq) { return 2 * (dq / 64) * kSubTileBytes; }
 __host__ __device__ constexpr int attn_stage_bytes(bool f8) { return f8 ? kNumStages * kStageBytes : 0; }

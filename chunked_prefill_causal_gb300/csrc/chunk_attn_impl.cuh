@@ -13,7 +13,7 @@
 // the merge kernel ("02 · 并行策略与 PP 切分" note, §7: partial results over
 // disjoint key ranges are combined through their LSE).
 //
-// CTA shape (384 threads, one CTA per SM):
+// CTA shape (384 threads over a bf16 cache, one CTA per SM):
 //   warp 0      TMA producer: the CTA's two 128-row query tiles once, then K
 //               and V tiles through a ring of 16 KB shared-memory slots (128
 //               keys x 64 dims each).  A K tile takes dq/64 consecutive slots
@@ -41,6 +41,9 @@
 //               row sum need no shuffles.  The TMA/MMA warpgroup runs on 64
 //               registers per thread so that the softmax threads get 216 and
 //               hold a whole 128-score row without spilling.
+//   Over an fp8 cache the CTA has 512 threads: warps 12-15 (one per SM
+//               sub-partition) copy the K/V codes into staging slots and widen
+//               them into the ring, and warpgroup 0 widens Q in place.
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+DV) O_B [256+DV,256+2DV).
 // P (bf16 pairs) overwrites the first 64 columns of its S tile.
 //
@@ -81,6 +84,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 constexpr int kRegsLow = 64;
 constexpr int kRegsHigh = 216;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch");
+// Over an fp8 cache (512 threads, 128 registers each at launch) the
+// converter warpgroup takes 40 and the softmax warpgroups 200.
+constexpr int kRegsConvF8 = 40;
+constexpr int kRegsHighF8 = 200;
+static_assert(128 * kRegsLow + 128 * kRegsConvF8 + 256 * kRegsHighF8 <= 512 * 128,
+              "fp8 register split exceeds the launch");
 constexpr uint64_t kCleanupNs = 100000000ull;  // 0.1 s for clean-up waits after an abort
 
 struct Ring {
@@ -101,9 +110,10 @@ struct Shape {
   static constexpr int NSLOT = attn_num_slots(DQ, F8);
   static constexpr int NB = NSLOT;     // tile barriers (>= tiles that fit the ring)
   static constexpr int NSTG = F8 ? kNumStages : 0;  // staging slots of E4M3 codes
-  static constexpr int NCONV = 2;                     // fp8: converter warps (0 and 2)
+  static constexpr int NCONV = 4;                     // fp8: converter warps 12..15
   static_assert(!F8 || (NSTG % NCONV == 0 && NB % 2 == 0),
                 "fp8: whole staging slots per converter; K tiles on even FULL barriers");
+  static constexpr int REGS_HIGH = F8 ? kRegsHighF8 : kRegsHigh;
   static constexpr int QBYTES = attn_q_bytes(DQ);
   // Operands are bf16, or f16 over an fp8 cache (E4M3 widens exactly to f16).
   static constexpr uint32_t IDESC_QK =
@@ -175,7 +185,7 @@ __device__ __forceinline__ void exps_to_tmem(const float (&sv)[128], float2 sl2,
 }  // namespace attn_detail
 
 template <int DQ, int DV, bool F8>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(attn_threads(F8), 1)
     chunk_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -232,9 +242,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(bar(S::B_TMP), 1);
     mbar_init(bar(S::B_END), 10);  // the 8 softmax warps and the 2 MMA issuers
     for (int i = 0; i < S::NB; ++i) {
-      // over an fp8 cache a tile is full once each of its sub-tiles is widened
+      // over an fp8 cache a tile is full once both halves of each of its
+      // sub-tiles are widened
       // (K tiles, even t, use even barriers)
-      mbar_init(bar(S::B_FULL + i), F8 ? ((i & 1) ? S::NVC : S::NQC) : 1);
+      mbar_init(bar(S::B_FULL + i), F8 ? 2 * ((i & 1) ? S::NVC : S::NQC) : 1);
       mbar_init(bar(S::B_EMPTY + i), 2);  // released by both MMA issuers
     }
     for (int i = 0; i < S::NSTG; ++i) mbar_init(bar(S::B_STG + i), 1);
@@ -256,63 +267,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp < 4) {
     regs_dec<kRegsLow>();
     if constexpr (F8) {
-      // ------------------------------------- producer over an fp8 cache
-      // The K/V codes of a sub-tile (128 keys x 64 dims) are copied by TMA
-      // into a staging slot, then warp 0 widens them exactly to f16 (each
-      // value times 2^-8, which the score scale and the final division undo)
-      // in the 128B-swizzled ring slot layout the MMAs read (the layout TMA
-      // writes for a bf16 cache), zeroing rows past the sequence (the pool
-      // holds whatever codes there), and signals the tile's FULL barrier.  Q is
-      // loaded as bf16 and turned into f16 in place by the 128 threads of
-      // this warpgroup before any MMA; the first staging copies are in flight
-      // meanwhile.
-      auto block_coord = [&](int b) -> int {
-        if (b * kBlockTokens >= seg.kv_len) return p.num_blocks;  // reads zeros
-        const int e = p.block_table[seg.table_off + b];
-        if (e < 0 || e >= p.num_blocks) {
-          record_status(p.status, kStatusInvalid);
-          return p.num_blocks;
-        }
-        return e;
-      };
-      constexpr int kPerPair = S::NQC + S::NVC;  // sub-tiles per K/V tile pair
-      constexpr int kSlotsPerWarp = S::NSTG / S::NCONV;
-      const int total = n_kv * kPerPair;
-      const int cw = warp >> 1;  // converter index of warps 0 and 2
-      // Sub-tile u (order K_0's, V_0's, K_1's, ...) is widened by converter
-      // u % NCONV through that warp's staging slots, in turn.
-      auto stage_slot = [&](int u) { return cw * kSlotsPerWarp + (u / S::NCONV) % kSlotsPerWarp; };
-      auto stage_parity = [&](int u) { return static_cast<uint32_t>((u / S::NCONV) / kSlotsPerWarp) & 1u; };
-      // Starts the copy of sub-tile u's codes into its staging slot (one lane).
-      auto issue_stage = [&](int u) {
-        const int j = u / kPerPair;
-        const int r = u - j * kPerPair;
-        const bool is_v = r >= S::NQC;
-        const int c = is_v ? r - S::NQC : r;
-        const int key0 = k_lo + j * kTileN;
-        int c0, c1;
-        if (p.paged) {
-          c0 = block_coord(key0 / kBlockTokens);
-          c1 = block_coord(key0 / kBlockTokens + 1);
-        } else {
-          c0 = seg.kv_base + key0;
-          c1 = c0 + kBlockTokens;
-        }
-        const int slot = stage_slot(u);
-        const uint32_t sb = bar(S::B_STG + slot);
-        const uint32_t d = smem_u32(sStage + slot * kStageBytes);
-        const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(sb, kStageBytes);
-        if (p.paged) {
-          tma_load_4d(d, m, sb, c * 64, g, 0, c0);
-          tma_load_4d(d + kStageBytes / 2, m, sb, c * 64, g, 0, c1);
-        } else {
-          tma_load_3d(d, m, sb, c * 64, g, c0);
-          tma_load_3d(d + kStageBytes / 2, m, sb, c * 64, g, c1);
-        }
-      };
-      const bool converter = (warp & 1) == 0 && cw < S::NCONV;
-      int issued = cw;  // next sub-tile whose staging copy this warp starts (lane 0)
+      // ------------------------------------- Q over an fp8 cache
+      // Q is loaded as bf16 and turned into f16 in place by the 128 threads
+      // of this warpgroup before any MMA (the converter warpgroup's first
+      // staging copies are in flight meanwhile).
       if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -323,8 +281,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_4d(smem_u32(sQ + (x * S::NQC + c) * kSubTileBytes), &tm_q, bar(S::B_Q),
                         c * 64, 0, g, seg.q_start + tok0 + x * T);
       }
-      if (converter && lane == 0)
-        for (int n = 0; n < kSlotsPerWarp && issued < total; ++n, issued += S::NCONV) issue_stage(issued);
       const bool qok = warp_wait(bar(S::B_Q), 0, p.status, abort_flag);
       if (qok) {
         // bf16 -> f16, 16 bytes per step; an element outside f16's range
@@ -345,66 +301,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       fence_proxy_async_smem();
       asm volatile("bar.sync 1, 128;" ::: "memory");  // the four warps of this warpgroup
-      if (converter) {
-        bool ok = qok;
-        int rq = 0;     // next tile whose release has not been observed
-        int done = cw;  // next sub-tile of this warp whose staging slot is not consumed
-        for (int u = cw; ok && u < total; u += S::NCONV) {
-          const int j = u / kPerPair;
-          const int r = u - j * kPerPair;
-          const int part = r >= S::NQC ? 1 : 0;
-          const int c = part ? r - S::NQC : r;
-          const int t = 2 * j + part;
-          const int pos = S::tile_pos(t);
-          const int nsub = S::tile_slots(t);
-          // Tiles are released in load order: wait until every tile that used
-          // these slots, and the tile that last used this barrier, is
-          // released.
-          while (rq < t && (rq <= t - S::NB || S::tile_pos(rq) < pos + nsub - S::NSLOT)) {
-            if (!(ok = warp_wait(bar(S::B_EMPTY + rq % S::NB), (rq / S::NB) & 1u, p.status, abort_flag)))
-              break;
-            ++rq;
-          }
-          if (!ok) break;
-          const int slot = stage_slot(u);
-          if (!(ok = warp_wait(bar(S::B_STG + slot), stage_parity(u), p.status, abort_flag))) break;
-          const uint8_t* src = sStage + slot * kStageBytes;
-          uint8_t* dst = sRing + ((pos + c) % S::NSLOT) * kSubTileBytes;
-          const int valid_rows = seg.kv_len - (k_lo + j * kTileN);
-#pragma unroll 4
-          for (int it = 0; it < kTileN * 4 / 32; ++it) {
-            const int idx = it * 32 + lane;
-            const int row = idx >> 2;  // key within the tile
-            const int q4 = idx & 3;    // 16 codes: dims 16 q4 .. 16 q4 + 15
-            uint4 w = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
-            if (row >= valid_rows) w = make_uint4(0u, 0u, 0u, 0u);
-            uint32_t h[8];
-            widen_e4m3x4_scaled(w.x, h[0], h[1]);
-            widen_e4m3x4_scaled(w.y, h[2], h[3]);
-            widen_e4m3x4_scaled(w.z, h[4], h[5]);
-            widen_e4m3x4_scaled(w.w, h[6], h[7]);
-            uint8_t* rp = dst + row * 128;
-            *reinterpret_cast<uint4*>(rp + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(rp + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          done = u + S::NCONV;
-          if (lane == 0) {
-            mbar_arrive(bar(S::B_FULL + t % S::NB));  // one of the tile's nsub arrivals
-            if (issued < total) {
-              issue_stage(issued);
-              issued += S::NCONV;
-            }
-          }
-        }
-        if (!ok && lane == 0) {
-          // Let every copy this warp started land before the CTA exits.
-          for (int v = done; v < issued; v += S::NCONV)
-            mbar_wait_for(bar(S::B_STG + stage_slot(v)), stage_parity(v), kCleanupNs);
-        }
-        if (!qok && warp == 0 && lane == 0) mbar_wait_for(bar(S::B_Q), 0, kCleanupNs);
-      }
+      if (!qok && warp == 0 && lane == 0) mbar_wait_for(bar(S::B_Q), 0, kCleanupNs);
     }
     if (!F8 && warp == 0 && lane == 0) {
       // ---------------------------------------------------- TMA producer
@@ -627,8 +524,118 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_wait_for(bar(S::B_FINAL + x), 0, kCleanupNs);
       }
     }
+  } else if (F8 && warp >= 12) {
+    if constexpr (F8) {
+      regs_dec<kRegsConvF8>();
+      // ---------------------------------- converters over an fp8 cache
+      // Warps 12..15, one per SM sub-partition.  The K/V codes of a half
+      // sub-tile (64 keys = one cache block x 64 dims) are copied by TMA into
+      // one of the warp's two staging slots; the warp widens them exactly to
+      // f16 (each value times 2^-8, which the score scale and the final
+      // division undo) into the 128B-swizzled ring slot layout the MMAs read
+      // (the layout TMA writes for a bf16 cache), zeroing rows past the
+      // sequence (the pool holds whatever codes there), and arrives on the
+      // tile's FULL barrier.  Unit u (order: K_0's half sub-tiles, V_0's, K_1's,
+      // ...) is widened by converter u % NCONV.
+      auto block_coord = [&](int b) -> int {
+        if (b * kBlockTokens >= seg.kv_len) return p.num_blocks;  // reads zeros
+        const int e = p.block_table[seg.table_off + b];
+        if (e < 0 || e >= p.num_blocks) {
+          record_status(p.status, kStatusInvalid);
+          return p.num_blocks;
+        }
+        return e;
+      };
+      constexpr int kUnits = 2 * (S::NQC + S::NVC);  // half sub-tiles per K/V tile pair
+      constexpr int kSlotsPerWarp = S::NSTG / S::NCONV;
+      const int total = n_kv * kUnits;
+      const int cw = warp - 12;
+      auto stage_slot = [&](int u) { return cw * kSlotsPerWarp + (u / S::NCONV) % kSlotsPerWarp; };
+      auto stage_parity = [&](int u) { return static_cast<uint32_t>((u / S::NCONV) / kSlotsPerWarp) & 1u; };
+      // tile pair j, K (part 0) or V (part 1), 64-dim sub-tile c, 64-key half hh
+      auto unit = [&](int u, int& j, int& part, int& c, int& hh) {
+        j = u / kUnits;
+        const int r = u - j * kUnits;
+        hh = r & 1;
+        const int sub = r >> 1;
+        part = sub >= S::NQC ? 1 : 0;
+        c = part ? sub - S::NQC : sub;
+      };
+      // Starts the copy of unit u's codes into its staging slot (one lane).
+      auto issue_stage = [&](int u) {
+        int j, part, c, hh;
+        unit(u, j, part, c, hh);
+        const int key0 = k_lo + j * kTileN + hh * kBlockTokens;
+        const int slot = stage_slot(u);
+        const uint32_t sb = bar(S::B_STG + slot);
+        const uint32_t d = smem_u32(sStage + slot * kStageBytes);
+        const CUtensorMap* m = part ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(sb, kStageBytes);
+        if (p.paged)
+          tma_load_4d(d, m, sb, c * 64, g, 0, block_coord(key0 / kBlockTokens));
+        else
+          tma_load_3d(d, m, sb, c * 64, g, seg.kv_base + key0);
+      };
+      int issued = cw;  // next unit whose staging copy this warp starts (lane 0)
+      if (lane == 0)
+        for (int n = 0; n < kSlotsPerWarp && issued < total; ++n, issued += S::NCONV) issue_stage(issued);
+      bool ok = true;
+      int rq = 0;     // next tile whose release has not been observed
+      int done = cw;  // next unit of this warp whose staging slot is not consumed
+      for (int u = cw; ok && u < total; u += S::NCONV) {
+        int j, part, c, hh;
+        unit(u, j, part, c, hh);
+        const int t = 2 * j + part;
+        const int pos = S::tile_pos(t);
+        const int nsub = S::tile_slots(t);
+        // Tiles are released in load order: wait until every tile that used
+        // these slots, and the tile that last used this barrier, is released.
+        while (rq < t && (rq <= t - S::NB || S::tile_pos(rq) < pos + nsub - S::NSLOT)) {
+          if (!(ok = warp_wait(bar(S::B_EMPTY + rq % S::NB), (rq / S::NB) & 1u, p.status, abort_flag)))
+            break;
+          ++rq;
+        }
+        if (!ok) break;
+        const int slot = stage_slot(u);
+        if (!(ok = warp_wait(bar(S::B_STG + slot), stage_parity(u), p.status, abort_flag))) break;
+        const uint8_t* src = sStage + slot * kStageBytes;
+        uint8_t* dst = sRing + ((pos + c) % S::NSLOT) * kSubTileBytes + hh * kBlockTokens * 128;
+        const int valid_rows = seg.kv_len - (k_lo + j * kTileN + hh * kBlockTokens);
+#pragma unroll 4
+        for (int it = 0; it < kBlockTokens * 4 / 32; ++it) {
+          const int idx = it * 32 + lane;
+          const int row = idx >> 2;  // key within the half (the swizzle phase is row & 7 either way)
+          const int q4 = idx & 3;    // 16 codes: dims 16 q4 .. 16 q4 + 15
+          uint4 w = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
+          if (row >= valid_rows) w = make_uint4(0u, 0u, 0u, 0u);
+          uint32_t h[8];
+          widen_e4m3x4_scaled(w.x, h[0], h[1]);
+          widen_e4m3x4_scaled(w.y, h[2], h[3]);
+          widen_e4m3x4_scaled(w.z, h[4], h[5]);
+          widen_e4m3x4_scaled(w.w, h[6], h[7]);
+          uint8_t* rp = dst + row * 128;
+          *reinterpret_cast<uint4*>(rp + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(rp + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        done = u + S::NCONV;
+        if (lane == 0) {
+          mbar_arrive(bar(S::B_FULL + t % S::NB));  // one of the tile's 2 nsub arrivals
+          if (issued < total) {
+            issue_stage(issued);
+            issued += S::NCONV;
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        // Let every copy this warp started land before the CTA exits.
+        for (int v = done; v < issued; v += S::NCONV)
+          mbar_wait_for(bar(S::B_STG + stage_slot(v)), stage_parity(v), kCleanupNs);
+      }
+    }
   } else {
-    regs_inc<kRegsHigh>();
+    regs_inc<S::REGS_HIGH>();
     // ------------------------------------------------------ softmax + epilogue
     const int x = (warp - 4) >> 2;
     const int wq = warp & 3;
@@ -836,7 +843,7 @@ cudaError_t launch_chunk_attn_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  chunk_attn_kernel<DQ, DV, F8><<<grid, kAttnThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+  chunk_attn_kernel<DQ, DV, F8><<<grid, attn_threads(F8), smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 
