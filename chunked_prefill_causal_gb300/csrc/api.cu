@@ -511,12 +511,10 @@ size_t widen_ws_bytes(const int32_t* cu, const int32_t* ctx, int32_t batch, int 
 }
 
 // Measured rates that split the SMs of a mixed batch: one decode CTA reads
-// about 80 GB/s of a bf16 cache (two fp8 CTAs share an SM, about 40 GB/s of
-// codes each); a prefill CTA does about 9.9 TFLOP/s on one SM with bf16
-// operands, about 4.1 reading E4M3 codes (widened in shared memory).
+// about 80 GB/s of a bf16 cache; a prefill CTA does about 9.9 TFLOP/s on one
+// SM.
 constexpr double kDecodeSmGBs = 80.0;
 constexpr double kPrefillSmTFlops = 9.9;
-constexpr double kPrefillSmTFlopsF8 = 4.1;
 
 // CTAs of the decode kernel in a mixed batch (0: one per work item).  The
 // decode rows are HBM-bound and the prefill segments tensor-bound, but a
@@ -526,15 +524,17 @@ constexpr double kPrefillSmTFlopsF8 = 4.1;
 // share is rounded up by 10%: a decode that ends last leaves SMs idle, and
 // the step time is flat over a range of shares around the best one.  A batch
 // without prefill segments, or whose decode needs nearly every SM anyway,
-// runs one CTA per work item.
-int mixed_decode_ctas(int num_sms, bool fp8, double prefill_flops, double decode_bytes, bool f8_prefill) {
-  if (prefill_flops <= 0.0 || decode_bytes <= 0.0 || num_sms < 2) return 0;
-  const double f = f8_prefill ? kPrefillSmTFlopsF8 : kPrefillSmTFlops;
-  const double r = (decode_bytes * f * 1e12) / (prefill_flops * kDecodeSmGBs * 1e9);
+// runs one CTA per work item.  So does a decode over an E4M3 pool: with every
+// SM it reads the codes at the copy bandwidth (9.25 GB in 1.4 ms for the
+// mixed workload), and running it first and the prefill after measured
+// faster than any share (6.25 against 8.6 ms with the prefill contexts
+// widened once, 9.9 against 10.4 ms widening in the kernel).
+int mixed_decode_ctas(int num_sms, bool fp8, double prefill_flops, double decode_bytes) {
+  if (fp8 || prefill_flops <= 0.0 || decode_bytes <= 0.0 || num_sms < 2) return 0;
+  const double r = (decode_bytes * kPrefillSmTFlops * 1e12) / (prefill_flops * kDecodeSmGBs * 1e9);
   const double sms = 1.1 * num_sms * r / (1.0 + r);
   if (sms >= 0.9 * num_sms) return 0;
-  const int d = std::max(1, (int)std::ceil(sms));
-  return fp8 ? 2 * d : d;
+  return std::max(1, (int)std::ceil(sms));
 }
 
 // CTAs of the top-k gather (0: one per work item).  Over a bf16 cache one
@@ -696,7 +696,7 @@ int mixed_impl(bool fp8, const void* q, const void* k_cache, const void* v_cache
   }
   for (int i = 0; i < nd; ++i)
     decode_bytes += (double)ctx_lens[drows[i]] * kv_heads * (head_dim_qk + head_dim_v) * (fp8 ? 1 : 2);
-  const int dctas = mixed_decode_ctas(ds->num_sms, fp8, prefill_flops, decode_bytes, fp8 && !widen);
+  const int dctas = mixed_decode_ctas(ds->num_sms, fp8, prefill_flops, decode_bytes);
   if (nd > 0 && launch_decode(dp, (int)dp_items, head_dim_qk, fp8, false, ds->num_sms, dctas, dst) != cudaSuccess)
     err = VPP_ERR_CUDA;
   if (fork && cudaEventRecord(ds->ev_join, ds->side) != cudaSuccess) err = VPP_ERR_CUDA;
