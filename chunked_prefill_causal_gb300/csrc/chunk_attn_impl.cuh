@@ -531,8 +531,7 @@ __global__ void __launch_bounds__(attn_threads(F8), 1)
       // Warps 12..15, one per SM sub-partition.  The K/V codes of a half
       // sub-tile (64 keys = one cache block x 64 dims) are copied by TMA into
       // one of the warp's two staging slots; the warp widens them exactly to
-      // f16 (each value times 2^-8, which the score scale and the final
-      // division undo) into the 128B-swizzled ring slot layout the MMAs read
+      // f16 into the 128B-swizzled ring slot layout the MMAs read
       // (the layout TMA writes for a bf16 cache), zeroing rows past the
       // sequence (the pool holds whatever codes there), and arrives on the
       // tile's FULL barrier.  Unit u (order: K_0's half sub-tiles, V_0's, K_1's,
@@ -609,10 +608,10 @@ __global__ void __launch_bounds__(attn_threads(F8), 1)
           uint4 w = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
           if (row >= valid_rows) w = make_uint4(0u, 0u, 0u, 0u);
           uint32_t h[8];
-          widen_e4m3x4_scaled(w.x, h[0], h[1]);
-          widen_e4m3x4_scaled(w.y, h[2], h[3]);
-          widen_e4m3x4_scaled(w.z, h[4], h[5]);
-          widen_e4m3x4_scaled(w.w, h[6], h[7]);
+          e4m3x4_to_f16x2x2(w.x, h[0], h[1]);
+          e4m3x4_to_f16x2x2(w.y, h[2], h[3]);
+          e4m3x4_to_f16x2x2(w.z, h[4], h[5]);
+          e4m3x4_to_f16x2x2(w.w, h[6], h[7]);
           uint8_t* rp = dst + row * 128;
           *reinterpret_cast<uint4*>(rp + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
           *reinterpret_cast<uint4*>(rp + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
@@ -648,10 +647,8 @@ __global__ void __launch_bounds__(attn_threads(F8), 1)
     const uint32_t tO = lane_base + 2 * kTileN + x * DV;
     // Per-kv-head factors of an fp8 cache (key codes x k_scale, values x
     // v_scale): k_scale joins the score scale, v_scale the final division.
-    // Over an fp8 cache the widened operands are the values times 2^-8.
-    constexpr float kWidenUndo = F8 ? 256.f : 1.f;
-    const float sl = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + g) * kWidenUndo : p.scale_log2;
-    const float vsc = p.v_scale ? __ldg(p.v_scale + g) * kWidenUndo : 1.f;
+    const float sl = p.k_scale ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
+    const float vsc = p.v_scale ? __ldg(p.v_scale + g) : 1.f;
     float m = -INFINITY;  // running max of score * scale * log2(e)
     float l = 0.f;        // running denominator, relative to 2^m
     bool ok = true;

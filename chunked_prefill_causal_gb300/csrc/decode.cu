@@ -83,16 +83,6 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// Four E4M3 codes (byte i of w = code i) -> two f16x2 words: lo holds codes 0
-// and 1, hi codes 2 and 3, the lower code in the lower half (exact: every
-// E4M3 value is an f16 value).
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
 // Two floats -> f16x2 (round to nearest even), `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;

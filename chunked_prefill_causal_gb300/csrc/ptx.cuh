@@ -331,23 +331,17 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ fp8 E4M3
-// Four E4M3 codes (byte i of w = code i) -> two f16x2 words (lo: codes 0, 1;
-// hi: codes 2, 3) holding each code's value times 2^-8, exactly.
-//
-// E4M3 (bias 7) and f16 (bias 15) put exponent and mantissa in the same
-// order, so the code's seven magnitude bits placed at f16 bits 7..13 give an
-// f16 whose exponent field is the code's and whose value is the code's value
-// scaled by 2^(7-15), for normal and subnormal codes alike (0 stays 0); the
-// sign moves from bit 7 to bit 15.  Integer operations only: each byte is
-// spread to its own 16-bit lane, x + (x & 0x80) moves the sign bit to bit 8
-// (no carry leaves the lane), and << 7 aligns both.  The NaN codes 0x7F and
-// 0xFF come out as +-480 instead (the append never writes them).
-__device__ __forceinline__ void widen_e4m3x4_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  uint32_t x0, x1;
-  asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(x0) : "r"(w));
-  asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(x1) : "r"(w));
-  lo = (x0 + (x0 & 0x00800080u)) << 7;
-  hi = (x1 + (x1 & 0x00800080u)) << 7;
+// Four E4M3 codes (byte i of w = code i) -> two f16x2 words: lo holds codes 0
+// and 1, hi codes 2 and 3, the lower code in the lower half (exact: every
+// E4M3 value is an f16 value).  One conversion instruction per two codes: in
+// both the chunk kernel's converter warps and the decode kernel it costs fewer
+// issue slots than spreading the bytes and moving the sign with integer
+// operations (which also widen exactly, to the values times 2^-8).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Two E4M3 codes (lo = the byte at the lower address) from two floats, round
