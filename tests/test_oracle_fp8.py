@@ -208,17 +208,17 @@ def test_unmutated_copy_passes_pins():
     assert _pins_pass(_module(_SRC, "fp8_copy"))
 
 
-def test_e4m3_bits_shifted_into_f16_are_the_value_times_2_to_the_minus_8():
-    # E4M3 (bias 7) and f16 (bias 15) order exponent and mantissa alike, so a
-    # code's seven magnitude bits placed at f16 bits 7..13, with its sign at
-    # bit 15, form an f16 equal to the code's value times 2^-8 -- subnormal
-    # codes and zeros included.  The fp8 attention kernels widen codes this
-    # way and undo the factor in their scales.
-    codes = np.arange(256, dtype=np.uint32)
-    bits = ((codes + (codes & 0x80)) << 7) & 0xFFFF
-    as_f16 = bits.astype(np.uint16).view(np.float16).astype(np.float64)
-    val = fp8.e4m3_decode(codes.astype(np.uint8)).astype(np.float64)
+def test_every_e4m3_value_is_an_f16_value():
+    # The fp8 attention kernels widen codes to f16 operands with a plain
+    # conversion and multiply by the scales afterwards; that is exact only if
+    # every finite E4M3 value (3 mantissa bits, exponents 2^-9 .. 2^8) is an
+    # f16 value (10 mantissa bits, subnormals down to 2^-24), signed zeros
+    # included.
+    codes = np.arange(256, dtype=np.uint8)
+    val = fp8.e4m3_decode(codes).astype(np.float64)
     finite = ~np.isnan(val)
     assert finite.sum() == 254
-    assert np.array_equal(as_f16[finite], val[finite] * 2.0 ** -8)
-    assert np.array_equal(np.signbit(as_f16[finite]), np.signbit(val[finite]))
+    as_f16 = val[finite].astype(np.float16)
+    assert np.array_equal(as_f16.astype(np.float64), val[finite])
+    assert np.array_equal(np.signbit(as_f16), np.signbit(val[finite]))
+    assert np.abs(val[finite]).max() == 448.0 and np.abs(val[finite][val[finite] != 0]).min() == 2.0 ** -9
