@@ -1182,6 +1182,81 @@ def run_mixed(args, dist_):
     return 0
 
 
+def timeline_intervals(buf, tiles=range(8, 60)):
+    """Median per-tile intervals (SM cycles) from one CTA's tracing-build
+    stamps [role][tile][event].  Roles 0/1 are the issuers of query tiles A/B;
+    their block j issues P V of tile j-1, then Q K^T of tile j (events: first
+    part of P(j-1) seen, turn taken, block issued, second part of P(j-1)
+    seen).  Roles 2/3 are the first softmax threads of A/B (events: S(j)
+    ready, S in registers, first part of P stored and signalled, second
+    part stored and signalled)."""
+    med = lambda xs: int(np.median(list(xs)))
+    out = {}
+    for x in range(2):
+        sm, iss = buf[2 + x], buf[x]
+        t = "AB"[x]
+        out[f"{t}.softmax: S ready -> S in registers"] = med(sm[j, 1] - sm[j, 0] for j in tiles)
+        out[f"{t}.softmax: S in registers -> first part of P signalled"] = med(sm[j, 2] - sm[j, 1] for j in tiles)
+        out[f"{t}.softmax: first -> second part of P signalled"] = med(sm[j, 3] - sm[j, 2] for j in tiles)
+        out[f"{t}.issuer: first part of P signalled -> seen"] = med(iss[j + 1, 0] - sm[j, 2] for j in tiles)
+        out[f"{t}.issuer: seen -> turn"] = med(iss[j + 1, 1] - iss[j + 1, 0] for j in tiles)
+        out[f"{t}.issuer: turn -> second part of P seen"] = med(iss[j + 1, 3] - iss[j + 1, 1] for j in tiles)
+        out[f"{t}.issuer: second part seen -> block issued"] = med(iss[j + 1, 2] - iss[j + 1, 3] for j in tiles)
+        out[f"{t}.issuer: block issued -> S ready"] = med(sm[j + 1, 0] - iss[j + 1, 2] for j in tiles)
+        out[f"{t}.period (S ready to S ready)"] = med(sm[j + 1, 0] - sm[j, 0] for j in tiles)
+    return out
+
+
+def run_timeline(args):
+    """Builds a copy of the library with -DVPP_TIMELINE=<cta> beside the
+    product one (the d 128 kernel then records clock64 stamps for CTA 0 and
+    CTA <cta>), runs one chunk of a workload unsplit, and prints the kernel
+    time and the median per-tile intervals as one JSON object."""
+    import ctypes
+    from chunked_prefill_causal_gb300 import build as B, vpp
+    out_dir = os.path.join(ROOT, "chunked_prefill_causal_gb300", "_build_timeline")
+    lib = vpp.load(B.build(extra_flags=(f"-DVPP_TIMELINE={args.timeline_cta}",), out_dir=out_dir,
+                           lib_name="libvpp_timeline.so"))
+    lib.vpp_timeline_read.argtypes = [ctypes.c_void_p]
+    lib.vpp_timeline_clear.argtypes = []
+    w = W.WORKLOADS[args.workload]
+    if (w.head_dim_qk, w.head_dim_v) != (128, 128):
+        raise SystemExit("--timeline: the stamps are compiled into the d 128 kernel only")
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    P, C = w.chunks()[args.timeline]
+    nb = W.blocks_for(P + C)
+    table = torch.from_numpy(W.block_table(nb, nb + 8, w.seed + 99)).to(dev)
+    kc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_qk), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros((nb + 8, 64, w.kv_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    q = None
+    for ci, (p0, _c0) in enumerate(w.chunks()[: args.timeline + 1]):
+        qi, ki, vi = W.chunk_tensors(w, ci, dev)
+        vpp.vpp_kv_append(ki, vi, kc, vc, p0, block_table=table)
+        q = qi
+        del ki, vi
+    out = torch.empty((C, w.heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    run = lambda: vpp.vpp_chunk_attn_ex(q, kc, vc, P, block_table=table, out=out, num_splits=1)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    if lib.vpp_timeline_clear() != 0:
+        raise RuntimeError("timeline clear failed")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    run()
+    e1.record()
+    torch.cuda.synchronize()
+    buf = np.zeros((2, 4, 64, 4), dtype=np.int64)
+    if lib.vpp_timeline_read(buf.ctypes.data_as(ctypes.c_void_p)) != 0:
+        raise RuntimeError("timeline read failed")
+    res = {"workload": w.name, "chunk": args.timeline, "prefix": P, "chunk_len": C,
+           "kernel_ms": round(e0.elapsed_time(e1), 3), "cta0": timeline_intervals(buf[0]),
+           f"cta{args.timeline_cta}": timeline_intervals(buf[1])}
+    print(json.dumps(res, indent=1))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1204,8 +1279,13 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the chunk kernel from an ncu capture")
+    ap.add_argument("--timeline", type=int, default=None, metavar="CHUNK",
+                    help="trace one chunk of the workload with the clock64-stamp build of the d 128 kernel")
+    ap.add_argument("--timeline-cta", type=int, default=500)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.timeline is not None:
+        return run_timeline(args)
     dist_ = Dist()
     if args.impl == "reference":
         if args.workload in ("mixed", "topk"):
