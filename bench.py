@@ -42,7 +42,7 @@ METRIC = "chunk-attn TFLOP/s & % BF16 tensor peak vs chunk index; prefill tokens
 # over the 8 launches of one long128k step, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only for the kernel sources whose
 # digest is recorded with it; any change to them makes the figure stale (null).
-TRAFFIC = {"long128k": {"sources_sha256": "e155e604b8d6381064073f9db3dc6b2079868afce270352a9e09b9f1a50a3ebb", "bytes_per_launch": 1.2052e9}}
+TRAFFIC = {"long128k": {"sources_sha256": "83c21427d4320d7fd32e41bfa222dfc8ce86417cd0bfd8eeadb43e13dee4f593", "bytes_per_launch": 1.1879e9}}
 KERNEL_SOURCES = ["chunk_attn_impl.cuh", "chunk_attn.cuh", "ptx.cuh"]
 
 
