@@ -61,3 +61,30 @@ def test_summary_keeps_the_judged_figures_in_a_short_tail():
     assert s["mixed_frac_of_bound"] == 0.5446 and s["append_frac_hbm"] == 0.99
     import json
     assert len(json.dumps(s)) < 1400
+
+
+def test_timeline_intervals_pair_each_issuer_block_with_the_previous_tiles_softmax():
+    import numpy as np
+    # Synthetic stamps with a 3000-cycle period: softmax of tile j at
+    # S ready 3000 j, S in registers +70, first part of P +600, second +1000;
+    # the issuer's block j (P V of tile j-1, then Q K^T of tile j) sees the
+    # first part at 3000 (j-1) + 800, takes the turn at +1000, sees the second
+    # part at +1500 and finishes issuing at +2900.
+    buf = np.zeros((4, 64, 4), dtype=np.int64)
+    for j in range(64):
+        for r in (2, 3):
+            buf[r, j] = [3000 * j, 3000 * j + 70, 3000 * j + 600, 3000 * j + 1000]
+        for r in (0, 1):
+            base = 3000 * (j - 1)
+            buf[r, j] = [base + 800, base + 1000, base + 2900, base + 1500]
+    iv = bench.timeline_intervals(buf)
+    for t in "AB":
+        assert iv[f"{t}.softmax: S ready -> S in registers"] == 70
+        assert iv[f"{t}.softmax: S in registers -> first part of P signalled"] == 530
+        assert iv[f"{t}.softmax: first -> second part of P signalled"] == 400
+        assert iv[f"{t}.issuer: first part of P signalled -> seen"] == 200
+        assert iv[f"{t}.issuer: seen -> turn"] == 200
+        assert iv[f"{t}.issuer: turn -> second part of P seen"] == 500
+        assert iv[f"{t}.issuer: second part seen -> block issued"] == 1400
+        assert iv[f"{t}.issuer: block issued -> S ready"] == 100
+        assert iv[f"{t}.period (S ready to S ready)"] == 3000
