@@ -368,3 +368,29 @@ def test_fp8_mixed_prefill_and_decode(widen):
     ctx = [300, 700, 64, 129, 1, 2000, 513, 4100]
     qlen = [300, 128, 1, 1, 1, 1, 77, 1]
     _mixed(ctx, qlen, 8, 2, 128, seed=77, widen=widen)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("case", [(8, 8, 128, 128, 1500, 300), (16, 2, 128, 128, 1500, 300),
+                                  (4, 4, 192, 128, 1300, 260)], ids=lambda c: "H%d-%d_d%d-%d_P%d_C%d" % c)
+def test_fp8_chunk_attention_with_growing_scores(case, splits):
+    # The running maximum moves on many tiles (keys grow with their position
+    # and each 128-key tile holds a needle ~20 log2 units above the last), with
+    # the codes widened inside the kernel: the reference, the denominator and
+    # the output accumulator must move together over the widened operands.
+    from tests.test_gpu_rescale import growing_scores
+    Hq, Hkv, dq, dv, P, C = case
+    q, k, v = growing_scores(P + C, Hq, Hkv, dq, dv, seed=Hq * 5 + dq)
+    ks, vs = amax_scales(k), amax_scales(v)
+    cache = Fp8Cache(k, v, ks, vs, seed=splits, append_chunk=400)
+    lse = torch.empty((Hq, C), dtype=torch.float32, device=DEV)
+    out = vpp.vpp_chunk_attn_fp8(q[P:].to(DEV), cache.k, cache.v, cache.ks, cache.vs, P, block_table=cache.table,
+                                 lse=lse, num_splits=splits)
+    torch.cuda.synchronize()
+    assert vpp.vpp_last_device_status() == 0
+    kq = ofp8.dequantize_kv(ofp8.quantize_kv(k.float().numpy(), ks), ks)
+    vq = ofp8.dequantize_kv(ofp8.quantize_kv(v.float().numpy(), vs), vs)
+    ref, ref_lse = oracle.causal_chunk_attention(to_np64(q[P:]), kq, vq, P)
+    assert ref_lse[:, -1].max() / math.log(2) > 100
+    assert_close(to_np64(out), ref)
+    assert np.abs(to_np64(lse) - ref_lse).max() <= LSE_ABS
