@@ -521,14 +521,15 @@ constexpr double kPrefillSmTFlops = 9.9;
 // kernel that starts first takes every SM.  So the decode kernel runs on a
 // fixed share of the SMs, the one where both would finish together, and the
 // prefill CTAs fill the rest (and the decode's SMs once it is done).  The
-// share is rounded up by 10%: a decode that ends last leaves SMs idle, and
-// the step time is flat over a range of shares around the best one.  A batch
-// without prefill segments, or whose decode needs nearly every SM anyway,
-// runs one CTA per work item.  So does a decode over an E4M3 pool: with every
-// SM it reads the codes at the copy bandwidth (9.25 GB in 1.4 ms for the
-// mixed workload), and running it first and the prefill after measured
-// faster than any share (6.25 against 8.6 ms with the prefill contexts
-// widened once, 9.9 against 10.4 ms widening in the kernel).
+// share is rounded up by 10%: a decode that ends last leaves SMs idle (on
+// the mixed workload, factors 0.9 / 1.0 / 1.1 / 1.2 / 1.3 / 1.5 measured
+// 6.79 / 6.31 / 6.03 / 6.27 / 6.50 / 6.38 ms).  A batch without prefill
+// segments, or whose decode needs nearly every SM anyway, runs one CTA per
+// work item.  So does a decode over an E4M3 pool: with every SM it reads the
+// codes at the copy bandwidth (9.25 GB in 1.4 ms for the mixed workload), and
+// running it first and the prefill after measured as fast as the best share
+// or faster (6.25 against 8.6 ms with the prefill contexts widened once; 8.81
+// against 8.75-20.5 ms over factors 0.5-1.6 widening in the kernel).
 int mixed_decode_ctas(int num_sms, bool fp8, double prefill_flops, double decode_bytes) {
   if (fp8 || prefill_flops <= 0.0 || decode_bytes <= 0.0 || num_sms < 2) return 0;
   const double r = (decode_bytes * kPrefillSmTFlops * 1e12) / (prefill_flops * kDecodeSmGBs * 1e9);
